@@ -1,0 +1,217 @@
+"""Float64 CPU oracle for the Mamba (S6) selective-scan forward pass.
+
+TEST INFRASTRUCTURE ONLY.  This package is the slow, obviously correct
+reference that the CUDA kernels are checked against.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it.  It shares no code with the CUDA path and never imports it.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, IEEE double, libm
+``exp``/``expm1``/``log1p``, OpenMP over independent channels).  This module
+only loads that library, widens the stored input values (fp32, or bf16 given
+as its raw 16-bit patterns) exactly to float64, and slices inputs.
+
+Sources: the pages "State-space models" (rayaq.ca; sections Discretization,
+Recurrence and convolution, Mamba: selection, Implementation) and
+"Structured State Space Models and Mamba" (llms.blog; sections Discretization
+Mechanics, the S6 section, Hardware-Aware Parallel Associative Scan).
+
+Every function here is pinned in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+RULE_EULER, RULE_BILINEAR, RULE_ZOH, RULE_ZOH_SIMPLE = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into liboracle.so (gcc, -O2, OpenMP, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # SSM_ORACLE_LIB lets the mutation test load a deliberately broken
+            # copy of this library in a child process.
+            lib = ctypes.CDLL(os.environ.get("SSM_ORACLE_LIB") or build())
+            d, i64, i32 = ctypes.c_double, ctypes.c_int64, ctypes.c_int
+            pd = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_softplus.restype = d
+            lib.oracle_softplus.argtypes = [d]
+            lib.oracle_discretize_scalar.restype = i32
+            lib.oracle_discretize_scalar.argtypes = [d, d, d, i32, pd, pd]
+            lib.oracle_selective_scan_f64.restype = i32
+            lib.oracle_selective_scan_f64.argtypes = (
+                [pd] * 10 + [i64] * 4 + [i32] * 5)
+            lib.oracle_lti_kernel.restype = i32
+            lib.oracle_lti_kernel.argtypes = [pd] * 5 + [i64] * 3 + [i32]
+            lib.oracle_causal_conv.restype = i32
+            lib.oracle_causal_conv.argtypes = [pd] * 4 + [i64] * 3 + [i32]
+            lib.oracle_max_threads.restype = i32
+            lib.oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def widen(a, io_dtype: str = "f32") -> np.ndarray:
+    """Exact float64 copy of stored values.
+
+    ``io_dtype == "bf16"``: ``a`` holds raw bfloat16 bit patterns (uint16);
+    a bfloat16 is the top half of a float32, so the value is the uint16
+    shifted into the high 16 bits of a float32 word.
+    """
+    if a is None:
+        return None
+    a = np.asarray(a)
+    if io_dtype == "bf16":
+        assert a.dtype == np.uint16, "bf16 values are passed as uint16 bit patterns"
+        f32 = (a.astype(np.uint32) << 16).view(np.float32)
+        return np.ascontiguousarray(f32, dtype=np.float64)
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def softplus(v: float) -> float:
+    """log(1 + e^v), evaluated in double."""
+    return float(_load().oracle_softplus(float(v)))
+
+
+def discretize(a: float, b: float, dt: float, rule: int):
+    """Scalar (abar, bbar) for h' = a h + b u with step dt.
+
+    rule: RULE_EULER, RULE_BILINEAR, RULE_ZOH (exact), RULE_ZOH_SIMPLE
+    (abar = e^{dt a}, bbar = dt b).
+    """
+    ab, bb = ctypes.c_double(), ctypes.c_double()
+    rc = _load().oracle_discretize_scalar(float(a), float(b), float(dt), int(rule),
+                                          ctypes.byref(ab), ctypes.byref(bb))
+    if rc != 0:
+        raise ValueError(f"unknown discretisation rule {rule}")
+    return ab.value, bb.value
+
+
+def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
+                   *, delta_softplus: bool = True, bbar_mode: int = 0,
+                   per_channel_bc: bool = False, io_dtype: str = "f32",
+                   threads: int = 0):
+    """Run the selective scan in float64.
+
+    Shapes: x, delta, z: (batch, L, dim); A: (dim, N); B, C: (batch, L, N), or
+    (dim, N) with ``per_channel_bc``; D, delta_bias: (dim,); h0: (batch, dim, N).
+    ``io_dtype`` says how x, delta, z and time-varying B, C are stored ("f32"
+    or "bf16" as uint16 bits); A, D, delta_bias, h0 and per-channel B, C are
+    always fp32/fp64 values.
+    Returns (out, final_state) as float64 arrays.
+    """
+    x64 = widen(x, io_dtype)
+    dl64 = widen(delta, io_dtype)
+    z64 = widen(z, io_dtype)
+    bc_dtype = "f32" if per_channel_bc else io_dtype
+    B64, C64 = widen(B, bc_dtype), widen(C, bc_dtype)
+    A64, D64, bias64 = widen(A), widen(D), widen(delta_bias)
+    batch, L, dim = x64.shape
+    N = A64.shape[1]
+    assert dl64.shape == x64.shape and A64.shape == (dim, N)
+    if per_channel_bc:
+        assert B64.shape == (dim, N) and C64.shape == (dim, N)
+    else:
+        assert B64.shape == (batch, L, N) and C64.shape == (batch, L, N)
+    if z64 is not None:
+        assert z64.shape == x64.shape
+    state = (np.array(h0, dtype=np.float64, order="C", copy=True) if h0 is not None
+             else np.zeros((batch, dim, N), dtype=np.float64))
+    assert state.shape == (batch, dim, N)
+    out = np.empty((batch, L, dim), dtype=np.float64)
+    rc = _load().oracle_selective_scan_f64(
+        _ptr(x64), _ptr(dl64), _ptr(A64), _ptr(B64), _ptr(C64), _ptr(D64),
+        _ptr(z64), _ptr(bias64), _ptr(out), _ptr(state),
+        batch, L, dim, N, int(per_channel_bc), int(delta_softplus),
+        int(h0 is not None), int(bbar_mode), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_selective_scan_f64 rejected its arguments")
+    return out, state
+
+
+def selective_scan_channels(channels, x, delta, A, B, C, D=None, z=None,
+                            delta_bias=None, h0=None, **kw):
+    """Scan only the listed channels ``[(b, d), ...]`` over the full length.
+
+    Inputs are sliced per batch row (no arithmetic); returns
+    ``{(b, d): (out[L], final_state[N])}``.
+    """
+    per_channel_bc = kw.get("per_channel_bc", False)
+    by_b = {}
+    for b, d in channels:
+        by_b.setdefault(int(b), []).append(int(d))
+    res = {}
+    for b, ds in by_b.items():
+        ds = sorted(set(ds))
+        sel = np.asarray(ds)
+        sl = lambda a: None if a is None else np.ascontiguousarray(a[b:b + 1][:, :, sel])
+        o, s = selective_scan(
+            sl(x), sl(delta), np.asarray(A)[sel],
+            np.asarray(B)[sel] if per_channel_bc else np.asarray(B)[b:b + 1],
+            np.asarray(C)[sel] if per_channel_bc else np.asarray(C)[b:b + 1],
+            None if D is None else np.asarray(D)[sel], sl(z),
+            None if delta_bias is None else np.asarray(delta_bias)[sel],
+            None if h0 is None else np.asarray(h0)[b:b + 1][:, sel], **kw)
+        for j, d in enumerate(ds):
+            res[(b, d)] = (o[0, :, j].copy(), s[0, j].copy())
+    return res
+
+
+def lti_kernel(A, B, C, dt, L: int, bbar_mode: int = 0):
+    """K[d, k] = sum_n C[d,n] e^{k dt_d A[d,n]} bbar[d,n], shape (dim, L)."""
+    A64, B64, C64, dt64 = widen(A), widen(B), widen(C), widen(dt)
+    dim, N = A64.shape
+    K = np.empty((dim, L), dtype=np.float64)
+    rc = _load().oracle_lti_kernel(_ptr(A64), _ptr(B64), _ptr(C64), _ptr(dt64),
+                                   _ptr(K), dim, N, L, int(bbar_mode))
+    if rc != 0:
+        raise ValueError("oracle_lti_kernel rejected its arguments")
+    return K
+
+
+def causal_conv(x, K, D=None, io_dtype: str = "f32", threads: int = 0):
+    """out[b,t,d] = sum_{k<=t} K[d,k] x[b,t-k,d] + D[d] x[b,t,d]."""
+    x64 = widen(x, io_dtype)
+    K64, D64 = widen(K), widen(D)
+    batch, L, dim = x64.shape
+    assert K64.shape == (dim, L)
+    out = np.empty_like(x64)
+    rc = _load().oracle_causal_conv(_ptr(x64), _ptr(K64), _ptr(D64), _ptr(out),
+                                    batch, L, dim, int(threads))
+    if rc != 0:
+        raise ValueError("oracle_causal_conv rejected its arguments")
+    return out

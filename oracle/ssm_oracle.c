@@ -1,0 +1,241 @@
+/*
+ * Float64 CPU oracle for the Mamba (S6) selective-scan forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * reference that the CUDA kernels are checked against.  Only the test suite,
+ * the package smoke check and the benchmark's CPU-baseline leg may load it;
+ * the product path never calls it and shares no code, header or table with
+ * it.  It steps the recurrence directly, in the order the pages state it,
+ * with no blocking, fusion or reordering.
+ *
+ * Sources (web pages on state-space models and Mamba):
+ *  - "State-space models" (rayaq.ca), sections "Discretization" (Euler,
+ *    bilinear, ZOH rules), "Recurrence and convolution" (unrolled sum from
+ *    h_{-1} = 0, kernel K_k = C Abar^k Bbar), "Mamba: selection" (softplus
+ *    step size, diagonal A, B_t and C_t shared by all channels) and
+ *    "Implementation" (shapes x, delta: (batch, L, D); A: (D, N);
+ *    B, C: (batch, L, N); h: (batch, D, N); the note that the fused scan uses
+ *    Bbar = delta * B).
+ *  - "Structured State Space Models and Mamba" (llms.blog), sections
+ *    "Discretization Mechanics" (h_k = Abar h_{k-1} + Bbar x_k,
+ *    y_k = C h_k + D x_k), "The Linear Time-Invariance Bottleneck and the
+ *    Selective State Space (S6)" (Delta_t = softplus(Linear(x_t) + bias))
+ *    and "Hardware-Aware Parallel Associative Scan".
+ *
+ * Every floating-point value is widened to double by the caller (the stored
+ * fp32 or bf16 values, exactly); all arithmetic here is IEEE double with the
+ * C library's exp / expm1 / log1p.
+ *
+ * Parity pins: every function here is pinned by tests/test_oracle_pins.py
+ * against the pages' worked examples, closed forms, the LTI convolution
+ * identity and brute force on tiny inputs.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(v) = log(1 + e^v), written so that neither branch overflows.
+ * ("State-space models", section "Mamba: selection": softplus keeps the step
+ * positive.) */
+double oracle_softplus(double v) {
+  return fmax(v, 0.0) + log1p(exp(-fabs(v)));
+}
+
+/* silu(z) = z * sigmoid(z), the output gate of the Mamba block
+ * ("State-space models", section "Mamba: selection", block description). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Scalar discretisation of h' = a h + b u with step dt
+ * ("State-space models", section "Discretization"):
+ *   rule 0  Euler:             abar = 1 + dt a,            bbar = dt b
+ *   rule 1  bilinear (Tustin): abar = (1 + dt a/2)/(1 - dt a/2),
+ *                              bbar = dt b / (1 - dt a/2)
+ *   rule 2  ZOH, exact:        abar = e^{dt a},            bbar = (e^{dt a} - 1)/a * b
+ *                              (limit dt b as a -> 0)
+ *   rule 3  ZOH with the simplified input term used by the fused scan:
+ *                              abar = e^{dt a},            bbar = dt b
+ * Returns 0, or -1 for an unknown rule. */
+int oracle_discretize_scalar(double a, double b, double dt, int rule,
+                             double* abar, double* bbar) {
+  switch (rule) {
+    case 0:
+      *abar = 1.0 + dt * a;
+      *bbar = dt * b;
+      return 0;
+    case 1: {
+      double left = 1.0 - 0.5 * dt * a;
+      *abar = (1.0 + 0.5 * dt * a) / left;
+      *bbar = dt * b / left;
+      return 0;
+    }
+    case 2:
+      *abar = exp(dt * a);
+      *bbar = (a != 0.0) ? expm1(dt * a) / a * b : dt * b;
+      return 0;
+    case 3:
+      *abar = exp(dt * a);
+      *bbar = dt * b;
+      return 0;
+    default:
+      return -1;
+  }
+}
+
+/*
+ * Selective scan, stepped directly.
+ *
+ * Layouts (row-major, contiguous):
+ *   x, delta, z, out : (batch, seqlen, dim)
+ *   A                : (dim, dstate)
+ *   B, C             : (batch, seqlen, dstate) when per_channel_bc == 0
+ *                      (time-varying, shared by every channel of a batch row)
+ *                      (dim, dstate) when per_channel_bc == 1 (LTI)
+ *   D, delta_bias    : (dim), either may be NULL (treated as 0)
+ *   z                : may be NULL (no gate)
+ *   state            : (batch, dim, dstate); read as h_{-1} when state_in,
+ *                      otherwise h_{-1} = 0; always overwritten with h_{L-1}.
+ *                      May be NULL when state_in == 0 (final state dropped).
+ *
+ * For each batch row b and channel d, with h = h_{-1}:
+ *   v     = delta[b,t,d] + bias[d]
+ *   dt    = softplus(v) if delta_softplus else v
+ *   abar  = exp(dt * A[d,n])
+ *   bbar  = dt * B[.,n]                       (bbar_mode 0)
+ *         = expm1(dt * A[d,n]) / A[d,n] * B   (bbar_mode 1, exact ZOH)
+ *   h[n]  = abar * h[n] + bbar * x[b,t,d]
+ *   y     = sum_n C[.,n] h[n] + D[d] x[b,t,d]
+ *   out   = y * silu(z[b,t,d])  (or y without a gate)
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_selective_scan_f64(const double* x, const double* delta,
+                              const double* A, const double* B,
+                              const double* C, const double* D,
+                              const double* z, const double* delta_bias,
+                              double* out, double* state, int64_t batch,
+                              int64_t seqlen, int64_t dim, int64_t dstate,
+                              int per_channel_bc, int delta_softplus,
+                              int state_in, int bbar_mode, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || dstate > 4096)
+    return -1;
+  if (state_in && state == NULL) return -1;
+  if (bbar_mode != 0 && bbar_mode != 1) return -1;
+  const int64_t nchan = batch * dim;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ch = 0; ch < nchan; ++ch) {
+    const int64_t b = ch / dim;
+    const int64_t d = ch % dim;
+    double h[4096];
+    for (int64_t n = 0; n < dstate; ++n)
+      h[n] = state_in ? state[(b * dim + d) * dstate + n] : 0.0;
+
+    for (int64_t t = 0; t < seqlen; ++t) {
+      const int64_t i = (b * seqlen + t) * dim + d; /* (b, t, d) */
+      const double v = delta[i] + (delta_bias ? delta_bias[d] : 0.0);
+      const double dt = delta_softplus ? oracle_softplus(v) : v;
+      const double xv = x[i];
+      const double* Bv = per_channel_bc ? &B[d * dstate]
+                                        : &B[(b * seqlen + t) * dstate];
+      const double* Cv = per_channel_bc ? &C[d * dstate]
+                                        : &C[(b * seqlen + t) * dstate];
+      double y = 0.0;
+      for (int64_t n = 0; n < dstate; ++n) {
+        const double a = A[d * dstate + n];
+        const double abar = exp(dt * a);
+        double bbar;
+        if (bbar_mode == 0)
+          bbar = dt * Bv[n];
+        else
+          bbar = (a != 0.0) ? expm1(dt * a) / a * Bv[n] : dt * Bv[n];
+        h[n] = abar * h[n] + bbar * xv;
+        y += Cv[n] * h[n];
+      }
+      y += (D ? D[d] : 0.0) * xv;
+      if (z) y *= silu(z[i]);
+      out[i] = y;
+    }
+    if (state)
+      for (int64_t n = 0; n < dstate; ++n)
+        state[(b * dim + d) * dstate + n] = h[n];
+  }
+  return 0;
+}
+
+/*
+ * Convolution kernel of a linear time-invariant diagonal SSM
+ * ("State-space models", section "Recurrence and convolution":
+ * K_k = C Abar^k Bbar).  Per channel d with constant step dt[d]:
+ *   K[d,k] = sum_n C[d,n] * exp(k * dt[d] * A[d,n]) * bbar[d,n],
+ * bbar = dt B (bbar_mode 0) or the exact ZOH term (bbar_mode 1).
+ * Abar^k is taken as exp(k dt a), its exact value for a diagonal A.
+ * K is (dim, seqlen).  Returns 0, or -1 on bad sizes.
+ */
+int oracle_lti_kernel(const double* A, const double* B, const double* C,
+                      const double* dt, double* K, int64_t dim,
+                      int64_t dstate, int64_t seqlen, int bbar_mode) {
+  if (dim < 0 || dstate <= 0 || seqlen < 0) return -1;
+  for (int64_t d = 0; d < dim; ++d) {
+    for (int64_t k = 0; k < seqlen; ++k) {
+      double s = 0.0;
+      for (int64_t n = 0; n < dstate; ++n) {
+        const double a = A[d * dstate + n];
+        const double bb = (bbar_mode == 0 || a == 0.0)
+                              ? dt[d] * B[d * dstate + n]
+                              : expm1(dt[d] * a) / a * B[d * dstate + n];
+        s += C[d * dstate + n] * exp((double)k * dt[d] * a) * bb;
+      }
+      K[d * seqlen + k] = s;
+    }
+  }
+  return 0;
+}
+
+/*
+ * Causal, zero-padded linear convolution of x with a per-channel kernel, plus
+ * the skip term ("State-space models", section "Recurrence and convolution";
+ * "Structured State Space Models and Mamba", LTI unroll
+ * y_k = sum_{j<=k} C Abar^{k-j} Bbar x_j):
+ *   out[b,t,d] = sum_{k=0..t} K[d,k] x[b,t-k,d] + D[d] x[b,t,d].
+ * x, out: (batch, seqlen, dim); K: (dim, seqlen); D may be NULL.
+ */
+int oracle_causal_conv(const double* x, const double* K, const double* D,
+                       double* out, int64_t batch, int64_t seqlen,
+                       int64_t dim, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const int64_t nchan = batch * dim;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ch = 0; ch < nchan; ++ch) {
+    const int64_t b = ch / dim;
+    const int64_t d = ch % dim;
+    for (int64_t t = 0; t < seqlen; ++t) {
+      double s = 0.0;
+      for (int64_t k = 0; k <= t; ++k)
+        s += K[d * seqlen + k] * x[(b * seqlen + (t - k)) * dim + d];
+      const int64_t i = (b * seqlen + t) * dim + d;
+      out[i] = s + (D ? D[d] : 0.0) * x[i];
+    }
+  }
+  return 0;
+}
+
+/* Number of threads OpenMP would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

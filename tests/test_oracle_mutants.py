@@ -1,0 +1,53 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake (a dropped term, a wrong sign, index or operand)
+in a copy of oracle/ssm_oracle.c, compiles it on the CPU, and runs the pin
+suite against it in a child process; the pins must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ssm_oracle.c")
+
+MUTANTS = {
+    "abar_sign": ("const double abar = exp(dt * a);", "const double abar = exp(-dt * a);"),
+    "input_dropped": ("h[n] = abar * h[n] + bbar * xv;", "h[n] = abar * h[n] + bbar;"),
+    "readout_uses_B": ("y += Cv[n] * h[n];", "y += Bv[n] * h[n];"),
+    "skip_dropped": ("y += (D ? D[d] : 0.0) * xv;", "y += 0.0 * xv;"),
+    "gate_no_sigmoid": ("if (z) y *= silu(z[i]);", "if (z) y *= z[i];"),
+    "softplus_sign": ("log1p(exp(-fabs(v)))", "log1p(exp(fabs(v)))"),
+    "bias_sign": ("delta[i] + (delta_bias ? delta_bias[d] : 0.0)", "delta[i] - (delta_bias ? delta_bias[d] : 0.0)"),
+    "B_time_shift": (": &B[(b * seqlen + t) * dstate];", ": &B[(b * seqlen + (t > 0 ? t - 1 : 0)) * dstate];"),
+    "state_in_ignored": ("h[n] = state_in ? state[(b * dim + d) * dstate + n] : 0.0;", "h[n] = 0.0;"),
+    "zoh_missing_div_a": ("bbar = (a != 0.0) ? expm1(dt * a) / a * Bv[n] : dt * Bv[n];",
+                          "bbar = (a != 0.0) ? expm1(dt * a) * Bv[n] : dt * Bv[n];"),
+    "A_state_reversed": ("const double a = A[d * dstate + n];\n        const double abar",
+                         "const double a = A[d * dstate + (dstate - 1 - n)];\n        const double abar"),
+    "conv_correlates": ("x[(b * seqlen + (t - k)) * dim + d]", "x[(b * seqlen + k) * dim + d]"),
+    "kernel_power_off_by_one": ("exp((double)k * dt[d] * a)", "exp((double)(k + 1) * dt[d] * a)"),
+    "bilinear_numerator_sign": ("*abar = (1.0 + 0.5 * dt * a) / left;", "*abar = (1.0 - 0.5 * dt * a) / left;"),
+    "euler_sign": ("*abar = 1.0 + dt * a;", "*abar = 1.0 - dt * a;"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "per_channel_C_row": ("const double* Cv = per_channel_bc ? &C[d * dstate]", "const double* Cv = per_channel_bc ? &C[0]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    orig, mutated = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation site for {name} not found exactly once"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(orig, mutated))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", str(lib),
+                    str(mpath), "-lm"], check=True)
+    env = dict(os.environ, SSM_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"

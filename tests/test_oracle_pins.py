@@ -1,0 +1,377 @@
+"""Pins for the float64 oracle: the pages' worked examples, closed forms,
+the LTI convolution identity, invariants, and brute force on tiny inputs.
+
+Each test names the page and section it checks.  None of them re-types the
+oracle's loop: every expected value comes from the pages, from a different
+formulation (closed-form sums, explicit products, library convolution,
+numerical quadrature) or from an identity the pages state.
+"""
+import functools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.metrics import floored_rel_err
+from selective_state_space_112_b300.workloads import (bf16_bits_to_f32, f32_to_bf16_bits,
+                                                      make_workload)
+
+
+def scalar_scan(u, a, b, c, step, bbar_mode, h0=None, d_skip=None):
+    """Drive the oracle with one channel and one state (LTI layout)."""
+    L = len(u)
+    x = np.asarray(u, dtype=np.float64).reshape(1, L, 1)
+    delta = np.full((1, L, 1), float(step))
+    out, st = oracle.selective_scan(
+        x, delta, np.array([[a]], float), np.array([[b]], float), np.array([[c]], float),
+        D=None if d_skip is None else np.array([d_skip], float),
+        h0=None if h0 is None else np.array([[[h0]]], float),
+        delta_softplus=False, bbar_mode=bbar_mode, per_channel_bc=True)
+    return out[0, :, 0], st[0, 0, 0]
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_zoh_worked_example(golden):
+    """'State Space Models: Mamba and Beyond', worked example of ZOH: printed
+    factors and outputs, and the analytic solution of dx/dt = -x + u."""
+    g = golden("zoh_worked_example.txt")
+    abar, bbar = oracle.discretize(g["A"], g["B"], g["step"], oracle.RULE_ZOH)
+    assert abs(abar - g["abar"]) < g["tol"] and abs(bbar - g["bbar"]) < g["tol"]
+    y, _ = scalar_scan(g["u"], g["A"], g["B"], g["C"], g["step"], bbar_mode=1)
+    assert np.max(np.abs(y - np.array(g["y"]))) < g["tol"]
+    # analytic trajectory: 1 - e^{-t} while u = 1 (t = 0.5, 1), then free decay
+    e = math.exp
+    analytic = [1 - e(-0.5), 1 - e(-1.0), (1 - e(-1.0)) * e(-0.5), (1 - e(-1.0)) * e(-1.0)]
+    assert np.max(np.abs(y - np.array(analytic))) < 1e-12
+
+
+def test_active_recall_answers(golden):
+    """'State Space Models: Mamba and Beyond', active-recall answers 1 and 2."""
+    g = golden("active_recall.txt")
+    abar, bbar = oracle.discretize(g["q1_A"], g["q1_B"], g["q1_step"], oracle.RULE_ZOH)
+    assert abs(abar - g["q1_abar"]) < g["tol"] and abs(bbar - g["q1_bbar"]) < g["tol"]
+    abar, bbar = oracle.discretize(g["q2_A"], g["q2_B"], g["q2_step"], oracle.RULE_ZOH)
+    assert abs(abar - g["q2_abar"]) < g["tol"] and abs(bbar - g["q2_bbar"]) < g["tol"]
+    y, _ = scalar_scan(g["q2_u"], g["q2_A"], g["q2_B"], 1.0, g["q2_step"], bbar_mode=1)
+    assert np.max(np.abs(y - np.array(g["q2_y"]))) < g["tol"]
+    # both step sizes sample the same continuous trajectory at t = 1 and t = 2
+    y_half, _ = scalar_scan([1, 1, 0, 0], -1.0, 1.0, 1.0, 0.5, bbar_mode=1)
+    assert abs(y[0] - y_half[1]) < 1e-14 and abs(y[1] - y_half[3]) < 1e-14
+
+
+def test_selection_worked_example(golden):
+    """'State Space Models: Mamba and Beyond', selection example: softplus
+    step and Abar = exp(step * A), pinned through the scan itself."""
+    g = golden("selection_worked_example.txt")
+    for v, step, abar in zip(g["pre_activation"], g["step"], g["abar"]):
+        assert abs(oracle.softplus(v) - step) < g["tol"]
+        # state 1, no input: one step leaves h = Abar
+        x = np.zeros((1, 1, 1))
+        dl = np.full((1, 1, 1), v)
+        _, st = oracle.selective_scan(x, dl, np.array([[g["A"]]]), np.ones((1, 1, 1)),
+                                      np.ones((1, 1, 1)), h0=np.ones((1, 1, 1)),
+                                      delta_softplus=True)
+        assert abs(st[0, 0, 0] - abar) < g["tol"]
+        # state 0, input 1, B = 1, Bbar = step * B: one step leaves h = step
+        _, st = oracle.selective_scan(np.ones((1, 1, 1)), dl, np.array([[g["A"]]]),
+                                      np.ones((1, 1, 1)), np.ones((1, 1, 1)),
+                                      delta_softplus=True)
+        assert abs(st[0, 0, 0] - step) < g["tol"]
+
+
+def test_softplus_against_library():
+    """softplus(v) = log(1 + e^v) (np.logaddexp), including far tails."""
+    for v in [-800.0, -40.0, -7.0, -0.5, 0.0, 1e-8, 1.0, 20.0, 40.0, 800.0]:
+        ref = float(np.logaddexp(0.0, v))
+        got = oracle.softplus(v)
+        assert abs(got - ref) <= 1e-15 * max(abs(ref), 1e-300) + 1e-320, (v, got, ref)
+
+
+# ----------------------------------------------------------- discretisation rules
+
+def test_discretization_factors(golden):
+    """'State-space models', Discretization: Euler, bilinear and ZOH factors."""
+    g = golden("discretization_factors.txt")
+    a = g["a"]
+    assert oracle.discretize(a, 1.0, 2.5, oracle.RULE_EULER)[0] == pytest.approx(g["euler_at_2.5"], abs=1e-15)
+    assert oracle.discretize(a, 1.0, 1.0, oracle.RULE_EULER)[0] == pytest.approx(g["euler_at_1"], abs=1e-15)
+    zoh = oracle.discretize(a, 1.0, 2.5, oracle.RULE_ZOH)[0]
+    assert 0.0 < zoh < 1.0 and zoh == pytest.approx(math.exp(-2.5), rel=1e-15)
+    # bilinear stays inside the unit circle for every step when a < 0
+    for dt in np.geomspace(1e-3, 1e3, 25):
+        assert abs(oracle.discretize(a, 1.0, dt, oracle.RULE_BILINEAR)[0]) < 1.0
+    # at step 0.1 bilinear is closer to the exact factor than Euler
+    ex = math.exp(-0.1)
+    bil = oracle.discretize(a, 1.0, 0.1, oracle.RULE_BILINEAR)[0]
+    eul = oracle.discretize(a, 1.0, 0.1, oracle.RULE_EULER)[0]
+    assert abs(bil - ex) < abs(eul - ex)
+    # bilinear is the (1,1) Pade approximant of e^x: error ~ |x|^3 / 12
+    x = -1e-3
+    bil = oracle.discretize(-1.0, 1.0, -x, oracle.RULE_BILINEAR)[0]
+    assert (bil - math.exp(x)) / x ** 3 == pytest.approx(1.0 / 12.0, rel=2e-3)
+    # Euler's input factor and the simplified ZOH input factor are step * b
+    assert oracle.discretize(a, 3.0, 0.25, oracle.RULE_EULER)[1] == pytest.approx(0.75, abs=1e-15)
+    assert oracle.discretize(a, 3.0, 0.25, oracle.RULE_ZOH_SIMPLE)[1] == pytest.approx(0.75, abs=1e-15)
+    # bilinear input factor: trapezoid-rule solution of h' = a h + b u with u = 1
+    ab, bb = oracle.discretize(-2.0, 1.0, 0.3, oracle.RULE_BILINEAR)
+    # trapezoid: h1 = h0 + dt/2 (a h0 + b + a h1 + b)  with h0 = 0  =>  h1 = dt b / (1 - dt a / 2)
+    assert bb == pytest.approx(0.3 / (1 + 0.3), rel=1e-14)
+    with pytest.raises(ValueError):
+        oracle.discretize(a, 1.0, 1.0, 7)
+
+
+def test_zoh_input_factor_is_integral():
+    """Exact ZOH input factor = integral_0^step e^{tau a} d tau * b
+    ('Structured State Space Models and Mamba', Discretization Mechanics)."""
+    from scipy.integrate import quad
+    for a, b, dt in [(-1.0, 1.0, 0.5), (-2.0, 0.7, 0.25), (-0.01, -1.3, 3.0), (-7.5, 2.0, 0.01)]:
+        integral, _ = quad(lambda tau: math.exp(tau * a), 0.0, dt, epsabs=0.0, epsrel=1e-13, limit=200)
+        _, bbar = oracle.discretize(a, b, dt, oracle.RULE_ZOH)
+        assert bbar == pytest.approx(integral * b, rel=1e-12)
+    # a -> 0 limit is step * b
+    assert oracle.discretize(0.0, 2.0, 0.3, oracle.RULE_ZOH)[1] == pytest.approx(0.6, rel=1e-15)
+    assert oracle.discretize(-1e-12, 2.0, 0.3, oracle.RULE_ZOH)[1] == pytest.approx(0.6, rel=1e-9)
+
+
+def test_small_and_large_step_limits():
+    """Small step: Abar -> 1 and Bbar -> 0 (token skipped); large step: Abar -> 0
+    ('State Space Models: Mamba and Beyond', answer 4; llms.blog, Discretization)."""
+    ab, bb = oracle.discretize(-1.0, 1.0, 1e-9, oracle.RULE_ZOH_SIMPLE)
+    assert abs(ab - 1.0) < 2e-9 and abs(bb) < 2e-9
+    ab, _ = oracle.discretize(-1.0, 1.0, 50.0, oracle.RULE_ZOH_SIMPLE)
+    assert 0 < ab < 1e-20
+    # through the scan: a tiny step keeps the state, a huge step erases it
+    x = np.ones((1, 1, 1))
+    _, st = oracle.selective_scan(x, np.full((1, 1, 1), 1e-9), np.array([[-1.0]]),
+                                  np.ones((1, 1)), np.ones((1, 1)), h0=np.full((1, 1, 1), 3.0),
+                                  delta_softplus=False, per_channel_bc=True)
+    assert st[0, 0, 0] == pytest.approx(3.0, rel=1e-8)
+    _, st = oracle.selective_scan(x, np.full((1, 1, 1), 60.0), np.array([[-1.0]]),
+                                  np.ones((1, 1)), np.ones((1, 1)), h0=np.full((1, 1, 1), 3.0),
+                                  delta_softplus=False, per_channel_bc=True, bbar_mode=1)
+    assert st[0, 0, 0] == pytest.approx(1.0, rel=1e-12)   # exact ZOH: state -> input
+
+
+# ------------------------------------------------------------------ closed forms
+
+def test_scalar_closed_form():
+    """h_t = sum_k a^k b x_{t-k} for constant a, b ('State-space models',
+    Recurrence and convolution), with the fused scan's Bbar = step * B."""
+    rng = np.random.default_rng(11)
+    L = 64
+    x = rng.standard_normal(L)
+    A, B, step = -0.7, 1.3, 0.2
+    a, b = math.exp(step * A), step * B
+    y, st = scalar_scan(x, A, B, 1.0, step, bbar_mode=0)
+    ref = np.array([sum(a ** k * b * x[t - k] for k in range(t + 1)) for t in range(L)])
+    assert floored_rel_err(y, ref) < 1e-13
+    assert st == pytest.approx(ref[-1], rel=1e-13)
+
+
+def test_lti_scan_equals_causal_convolution():
+    """LTI system: the recurrence equals causal convolution with
+    K_k = C Abar^k Bbar plus D x ('State-space models', Recurrence and
+    convolution; 'Structured State Space Models and Mamba', LTI unroll).
+    Abar^k is built by repeated multiplication, the convolution by np.convolve."""
+    w = make_workload("lti_small", batch=2, seqlen=512, dim=8, dstate=16, seed=1,
+                      a_init="s4d_real", gate=False, lti=True, with_bias=False)
+    out, _ = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D,
+                                   delta_softplus=False, per_channel_bc=True)
+    dt = w.delta[0, 0, :].astype(np.float64)
+    A, B, C = (w.A.astype(np.float64), w.B.astype(np.float64), w.C.astype(np.float64))
+    Abar = np.exp(dt[:, None] * A)                               # (dim, N)
+    powers = np.cumprod(np.concatenate([np.ones((w.dim, w.dstate, 1)),
+                                        np.repeat(Abar[:, :, None], w.seqlen - 1, axis=2)],
+                                       axis=2), axis=2)          # Abar^k, k = 0..L-1
+    K = np.einsum("dn,dnk,dn->dk", C, powers, dt[:, None] * B)
+    ref = np.empty_like(out)
+    for b in range(w.batch):
+        for d in range(w.dim):
+            xs = w.x[b, :, d].astype(np.float64)
+            ref[b, :, d] = np.convolve(xs, K[d])[: w.seqlen] + w.D[d] * xs
+    assert floored_rel_err(out, ref) < 1e-12
+    # the oracle's own kernel and O(L^2) convolution agree with the same identity
+    assert floored_rel_err(oracle.lti_kernel(w.A, w.B, w.C, dt, w.seqlen), K) < 1e-12
+    assert floored_rel_err(oracle.causal_conv(w.x, K, w.D), ref) < 1e-12
+
+
+def test_impulse_response_and_shift_invariance():
+    """Feeding 1, 0, 0, ... returns the kernel K ('State-space models',
+    Recurrence and convolution); the response to a later impulse is a
+    translated copy (rugvailabs page, S4D section)."""
+    w = make_workload("lti_imp", batch=1, seqlen=40, dim=3, dstate=4, seed=5,
+                      a_init="random", gate=False, lti=True, with_bias=False)
+    dt = w.delta[0, 0, :].astype(np.float64)
+    K = oracle.lti_kernel(w.A, w.B, w.C, dt, w.seqlen)
+    resp = {}
+    for s in (0, 7):
+        x = np.zeros_like(w.x)
+        x[0, s, :] = 1.0
+        out, _ = oracle.selective_scan(x, w.delta, w.A, w.B, w.C, D=w.D,
+                                       delta_softplus=False, per_channel_bc=True)
+        resp[s] = out[0]
+    expect = K.T.copy()
+    expect[0] += w.D
+    assert floored_rel_err(resp[0], expect) < 1e-13
+    assert np.all(resp[7][:7] == 0.0)
+    assert floored_rel_err(resp[7][7:], resp[0][: w.seqlen - 7]) < 1e-13
+
+
+# --------------------------------------------------------------- brute force
+
+def _brute_force(w, bbar_mode):
+    """h_t = (prod_{r<=t} Abar_r) h0 + sum_{s<=t} (prod_{r=s+1..t} Abar_r) Bbar_s x_s,
+    each product formed explicitly ('Structured State Space Models and Mamba',
+    parallel associative scan: the composition of the per-step maps)."""
+    f = (lambda a: bf16_bits_to_f32(a).astype(np.float64)) if w.io == "bf16" else \
+        (lambda a: np.asarray(a, dtype=np.float64))
+    x, dl = f(w.x), f(w.delta)
+    B = np.asarray(w.B, np.float64) if w.per_channel_bc else f(w.B)
+    C = np.asarray(w.C, np.float64) if w.per_channel_bc else f(w.C)
+    z = None if w.z is None else f(w.z)
+    A = w.A.astype(np.float64)
+    bias = np.zeros(w.dim) if w.delta_bias is None else w.delta_bias.astype(np.float64)
+    Dk = np.zeros(w.dim) if w.D is None else w.D.astype(np.float64)
+    out = np.zeros((w.batch, w.seqlen, w.dim))
+    fin = np.zeros((w.batch, w.dim, w.dstate))
+    for b in range(w.batch):
+        for d in range(w.dim):
+            v = dl[b, :, d] + bias[d]
+            step = np.logaddexp(0.0, v) if w.delta_softplus else v
+            for n in range(w.dstate):
+                abar = np.exp(step * A[d, n])
+                Bv = B[d, n] * np.ones(w.seqlen) if w.per_channel_bc else B[b, :, n]
+                if bbar_mode == 0:
+                    bbar = step * Bv
+                else:
+                    bbar = (abar - 1.0) / A[d, n] * Bv
+                Cv = C[d, n] * np.ones(w.seqlen) if w.per_channel_bc else C[b, :, n]
+                h0 = 0.0 if w.h0 is None else float(w.h0[b, d, n])
+                for t in range(w.seqlen):
+                    h = np.prod(abar[: t + 1]) * h0
+                    for s in range(t + 1):
+                        h += np.prod(abar[s + 1: t + 1]) * bbar[s] * x[b, s, d]
+                    out[b, t, d] += Cv[t] * h
+                    if t == w.seqlen - 1:
+                        fin[b, d, n] = h
+            out[b, :, d] += Dk[d] * x[b, :, d]
+            if z is not None:
+                out[b, :, d] *= z[b, :, d] / (1.0 + np.exp(-z[b, :, d]))
+    return out, fin
+
+
+@pytest.mark.parametrize("case", [
+    dict(io="f32", gate=True, state_in=False, a_init="random", bbar_mode=0),
+    dict(io="f32", gate=False, state_in=True, a_init="s4d_real", bbar_mode=0),
+    dict(io="bf16", gate=True, state_in=True, a_init="random", bbar_mode=0),
+    dict(io="f32", gate=True, state_in=True, a_init="random", bbar_mode=1),
+    dict(io="f32", gate=True, state_in=False, a_init="random", bbar_mode=0, with_D=False, with_bias=False),
+    dict(io="f32", gate=False, state_in=False, a_init="random", bbar_mode=1, lti=True, with_bias=False),
+])
+def test_brute_force_tiny(case):
+    case = dict(case)
+    bbar_mode = case.pop("bbar_mode")
+    w = make_workload("bf", batch=2, seqlen=11, dim=3, dstate=4, seed=17, **case)
+    out, fin = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                     delta_bias=w.delta_bias, h0=w.h0,
+                                     delta_softplus=w.delta_softplus, bbar_mode=bbar_mode,
+                                     per_channel_bc=w.per_channel_bc, io_dtype=w.io)
+    ref_out, ref_fin = _brute_force(w, bbar_mode)
+    assert floored_rel_err(out, ref_out) < 1e-13
+    assert floored_rel_err(fin, ref_fin) < 1e-13
+
+
+# ------------------------------------------------------------ scan algebra
+
+def _combine(p, q):
+    """(a1, b1) then (a2, b2) = (a1 a2, a2 b1 + b2)  ('State-space models',
+    The parallel scan; llms.blog, Hardware-Aware Parallel Associative Scan)."""
+    return (p[0] * q[0], q[0] * p[1] + q[1])
+
+
+def test_combine_is_associative():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        e = [(rng.uniform(0, 1), rng.standard_normal()) for _ in range(3)]
+        l = _combine(_combine(e[0], e[1]), e[2])
+        r = _combine(e[0], _combine(e[1], e[2]))
+        assert l[0] == pytest.approx(r[0], rel=1e-14) and l[1] == pytest.approx(r[1], rel=1e-12, abs=1e-14)
+
+
+def test_tree_scan_matches_oracle_state():
+    """A pairwise (tree-order) reduction of the per-step maps reaches the same
+    final state as the oracle's sequential recurrence."""
+    w = make_workload("tree", batch=1, seqlen=37, dim=2, dstate=3, seed=23, state_in=True)
+    _, fin = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                   delta_bias=w.delta_bias, h0=w.h0)
+    for d in range(w.dim):
+        step = np.logaddexp(0.0, w.delta[0, :, d].astype(np.float64) + float(w.delta_bias[d]))
+        for n in range(w.dstate):
+            elems = [(math.exp(s * float(w.A[d, n])), s * float(w.B[0, t, n]) * float(w.x[0, t, d]))
+                     for t, s in enumerate(step)]
+            while len(elems) > 1:
+                nxt = [_combine(elems[i], elems[i + 1]) for i in range(0, len(elems) - 1, 2)]
+                if len(elems) % 2:
+                    nxt.append(elems[-1])
+                elems = nxt
+            a_all, b_all = elems[0]
+            h = a_all * float(w.h0[0, d, n]) + b_all
+            assert h == pytest.approx(fin[0, d, n], rel=1e-12, abs=1e-14)
+
+
+# -------------------------------------------------------------- invariants
+
+def test_split_resume_equals_single_scan():
+    """Final state is a checkpoint: scan(L1) then scan(L2) from it = scan(L1 + L2)
+    (constant-size state at inference: rugvailabs page, comparison table)."""
+    w = make_workload("split", batch=2, seqlen=50, dim=4, dstate=5, seed=29, io="bf16")
+    kw = dict(D=w.D, delta_bias=w.delta_bias, io_dtype="bf16")
+    full, fin = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, z=w.z, **kw)
+    cut = 19
+    sl = lambda a, s: a[:, s]
+    o1, s1 = oracle.selective_scan(sl(w.x, slice(0, cut)), sl(w.delta, slice(0, cut)), w.A,
+                                   sl(w.B, slice(0, cut)), sl(w.C, slice(0, cut)),
+                                   z=sl(w.z, slice(0, cut)), **kw)
+    o2, s2 = oracle.selective_scan(sl(w.x, slice(cut, None)), sl(w.delta, slice(cut, None)), w.A,
+                                   sl(w.B, slice(cut, None)), sl(w.C, slice(cut, None)),
+                                   z=sl(w.z, slice(cut, None)), h0=s1, **kw)
+    assert np.array_equal(np.concatenate([o1, o2], axis=1), full)
+    assert np.array_equal(s2, fin)
+
+
+def test_zero_length_and_channel_sampling():
+    w = make_workload("z", batch=2, seqlen=0, dim=3, dstate=2, seed=1, state_in=True)
+    out, fin = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                     delta_bias=w.delta_bias, h0=w.h0)
+    assert out.shape == (2, 0, 3) and np.array_equal(fin, w.h0.astype(np.float64))
+    w = make_workload("s", batch=3, seqlen=9, dim=5, dstate=2, seed=2)
+    out, fin = oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                     delta_bias=w.delta_bias)
+    picks = [(0, 4), (2, 1), (2, 3)]
+    res = oracle.selective_scan_channels(picks, w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                         delta_bias=w.delta_bias)
+    for (b, d) in picks:
+        assert np.array_equal(res[(b, d)][0], out[b, :, d])
+        assert np.array_equal(res[(b, d)][1], fin[b, d])
+
+
+def test_workload_recipe():
+    """bias = log(expm1(dt)) is the value whose softplus is dt; bf16 rounding is
+    nearest-even; stored bf16 widens exactly."""
+    w = make_workload("r", batch=1, seqlen=4, dim=6, dstate=2, seed=0)
+    rng = np.random.Generator(np.random.PCG64(0))
+    rng.standard_normal((1, 4, 6), dtype=np.float32)
+    rng.standard_normal((1, 4, 6), dtype=np.float32)
+    dt = rng.uniform(0.001, 0.1, size=6)
+    for d in range(6):
+        assert oracle.softplus(float(w.delta_bias[d])) == pytest.approx(dt[d], rel=1e-6)
+    vals = np.array([1.0, 1.00390625, 1.005859375, 1.0078125 + 2 ** -9, -3.14159, 1e-30],
+                    dtype=np.float32)
+    bits = f32_to_bf16_bits(vals)
+    back = bf16_bits_to_f32(bits)
+    assert back[0] == 1.0 and back[1] == 1.0            # tie 1 + 2^-8 -> even mantissa (1.0)
+    assert back[2] == 1.0078125
+    assert np.all(np.abs(back - vals) <= np.abs(vals) * 2.0 ** -8)
+    assert np.array_equal(oracle.widen(bits, "bf16"), back.astype(np.float64))
