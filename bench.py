@@ -1,0 +1,372 @@
+"""Benchmark of the selective-scan forward on B300.
+
+One step = one ssm_selective_scan_fwd call over the whole workload (every row of
+the hot path: load, step size, discretisation, scan with chunk carries,
+readout + gate epilogue, final state).  Default workload: the long-context
+bf16 layer (batch 1, L = 131072, D = 2560, N = 16), whose inputs (2.69 GB) are
+larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (the scan shards over batch rows and channels with no
+exchange), so scaling is weak and `value` is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan tokens*channels/s"
+UNIT = "tokens*channels/s"
+FMA_LANES_PER_SM = 128      # FP32 FMA-pipe lanes per SM per clock (B300)
+FMA_SLOTS_PER_UPDATE = 6    # see alu roofline in the design doc: step*A, ex2 (2 slots), step*x*B, h, y
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk.get("sm_max_mhz", 2032.0)), "measured"
+    except Exception:
+        return 6400.0, 2032.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons while running: NVML when the Python
+    binding is importable, else `nvidia-smi -lms` in a background process."""
+
+    REASONS = {  # NVML clocks-event-reason bits
+        0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+    }
+
+    def __init__(self, local_rank: int, period_s: float = 0.005):
+        cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [c for c in cvd.split(",") if c.strip()]
+        self.index = int(ids[local_rank]) if local_rank < len(ids) and ids[local_rank].strip().isdigit() \
+            else local_rank
+        self.period = period_s
+        self.samples = []       # (mhz, reason bitmask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self._proc = None
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
+            self._t.start()
+            return self
+        except Exception:
+            pass
+        import subprocess
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._run_smi, daemon=True)
+            self._t.start()
+            time.sleep(0.3)  # let nvidia-smi start sampling before the timed work
+        except Exception:
+            self._proc = None
+        return self
+
+    def _run_nvml(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
+                                     nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            if self._stop.is_set():
+                break
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                mhz, mx = float(parts[0]), float(parts[1])
+                rs = int(parts[2], 16) if parts[2].startswith("0x") else int(parts[2])
+                self.max_mhz = mx
+                self.samples.append((mhz, rs))
+            except Exception:
+                continue
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "samples": 0}
+        seen = set()
+        for _, rs in self.samples:
+            for bit, name in self.REASONS.items():
+                if rs & bit:
+                    seen.add(name)
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(seen),
+                "samples": len(self.samples)}
+
+
+def device_tensors(w, torch, device):
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return {k: dev(getattr(w, k)) for k in ("x", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0")}
+
+
+def oracle_sample(w, k):
+    """The float64 oracle, as it stands, on channels 0..k-1 of batch row 0 over the
+    full sequence length; returns seconds."""
+    import oracle
+    t = time.perf_counter()
+    oracle.selective_scan_channels([(0, d) for d in range(k)], w.x, w.delta, w.A, w.B, w.C,
+                                   D=w.D, z=w.z, delta_bias=w.delta_bias, h0=w.h0,
+                                   delta_softplus=w.delta_softplus, io_dtype=w.io)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    import oracle
+    cores = oracle.max_threads()
+    cap = min(w.dim, 512)
+    k = min(cap, max(cores, 8))
+    t = oracle_sample(w, k)
+    k2 = int(min(cap, max(k, k * budget_s / max(t, 1e-3))))
+    k2 = max(1, (k2 // cores) * cores) if k2 >= cores else k2
+    if k2 > k:
+        t, k = oracle_sample(w, k2), k2
+    units = k * w.seqlen
+    return {"value": units / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, N={w.dstate} "
+                      f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from selective_state_space_112_b300.workloads import CONFIGS, make_workload
+    if args.workload not in CONFIGS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(CONFIGS)}")
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    import selective_state_space_112_b300 as ssm
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    spec = dict(CONFIGS[args.workload])
+    spec["seed"] = spec["seed"] + 1000 * rank  # independent replica per rank
+    w = make_workload(args.workload, **spec)
+    t = device_tensors(w, torch, device)
+    out = torch.empty_like(t["x"])
+    fs0 = t["h0"]
+    fs = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    state_in = w.h0 is not None
+
+    def step():
+        if state_in:
+            fs.copy_(fs0)  # recurrent-step workload: restore the stored state
+        ssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                   t["delta_bias"], out=out, final_state=fs,
+                                   delta_softplus=w.delta_softplus, state_in=state_in)
+
+    for _ in range(args.warmup):
+        step()
+    assert ssm.ssm_check_status() == 0
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, events on the launch stream, barrier + sync both sides
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ssm.ssm_kernel_launches()
+    ssm.ssm_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ssm.ssm_profile_enable(False)
+    prof = ssm.ssm_profile_read()
+    launches = ssm.ssm_kernel_launches() - launches0
+    assert ssm.ssm_check_status() == 0
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    ms_step = ms / args.steps
+    units = w.tokens_channels
+    value = world * units * args.steps / (ms * 1e-3)
+
+    # ---- roofline of the dominant kernel (CUDA events recorded around each launch)
+    hbm_peak, sm_max, peak_kind = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    alg = w.algorithmic_bytes()
+    dom = max(prof, key=lambda k: prof[k][1]) if prof else None
+    dom_ms = prof[dom][1] / prof[dom][0] if dom else ms_step
+    achieved = alg / (dom_ms * 1e-3) / 1e9
+    alu_peak = FMA_LANES_PER_SM * sms * sm_max * 1e6 / FMA_SLOTS_PER_UPDATE  # updates/s
+    alu_achieved = w.element_updates / (dom_ms * 1e-3)
+    total_ms = sum(v[1] for v in prof.values()) or 1.0
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
+            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "peak_source": peak_kind,
+            "traffic": None, "algorithmic_bytes_per_launch": alg,
+            "kernel_ms_avg": round(dom_ms, 4),
+            "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4),
+                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()},
+            "alu": {"achieved": alu_achieved, "peak": alu_peak, "unit": "state-updates/s",
+                    "frac": round(alu_achieved / alu_peak, 4),
+                    "peak_basis": f"{FMA_LANES_PER_SM} FP32 lanes/SM x {sms} SMs x {sm_max:.0f} MHz"
+                                  f" / {FMA_SLOTS_PER_UPDATE} FMA-pipe slots per state update"}}
+
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic",
+           "config": {"workload": args.workload, "batch": w.batch, "seqlen": w.seqlen,
+                      "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io,
+                      "gate": w.z is not None, "state_in": state_in,
+                      "parallelism": f"replica x{world}" if world > 1 else "single",
+                      "l2": f"inputs {alg / 1e9:.2f} GB > 126 MB L2; no flush needed"
+                            if alg > 4 * 126e6 else "L2 resident (latency case)"},
+           "hbm_gbs_step": round(alg / (ms_step * 1e-3) / 1e9, 1),
+           "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary()}
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in t.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            fsd = dev_in["h0"] if state_in else fs
+            ssm.ssm_selective_scan_fwd(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"],
+                                       dev_in["C"], dev_in["D"], dev_in["z"], dev_in["delta_bias"],
+                                       out=out, final_state=fsd,
+                                       delta_softplus=w.delta_softplus, state_in=state_in)
+            out_h.copy_(out, non_blocking=True)
+            fs_h.copy_(fsd, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ems], device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        res["e2e"] = {"value": world * units * args.e2e_steps / (ems * 1e-3), "unit": UNIT,
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": ems / args.e2e_steps}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: timed on the host cores, each step a
+    bounded sample of the same workload.  Under torchrun only rank 0 runs."""
+    if rank != 0:
+        return
+    from selective_state_space_112_b300.workloads import config
+    import oracle
+    w = config(args.workload)
+    cores = oracle.max_threads()
+    k = min(w.dim, max(cores, 8))
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(w, k)
+    el = 0.0
+    for _ in range(args.steps):
+        el += oracle_sample(w, k)
+    units = k * w.seqlen
+    value = units * args.steps / el
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "batch": w.batch, "seqlen": w.seqlen,
+                      "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps per step"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

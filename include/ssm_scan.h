@@ -1,0 +1,152 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) Mamba S6 selective-scan forward.
+ *
+ * The operation (pages "State-space models", rayaq.ca, sections
+ * "Discretization", "Mamba: selection", "The parallel scan" and
+ * "Implementation"; "Structured State Space Models and Mamba", llms.blog,
+ * sections "Discretization Mechanics", the S6 section and "The GPU Memory
+ * Hierarchy and Kernel Fusion"): for every batch row b, channel d, step t and
+ * state n,
+ *
+ *   step_t  = softplus(delta[b,t,d] + delta_bias[d])   (or without softplus)
+ *   Abar    = exp(step_t * A[d,n])                      zero-order hold, diagonal A
+ *   Bbar x  = step_t * B[.,t,n] * x[b,t,d]              the fused scan's input term
+ *   h_t[n]  = Abar * h_{t-1}[n] + Bbar x                h_{-1} = 0 or a given state
+ *   y_t     = sum_n C[.,t,n] h_t[n] + D[d] x[b,t,d]
+ *   out     = y_t * silu(z[b,t,d])                      when a gate z is given
+ *
+ * The expanded state (batch, L, dim, N) never reaches device memory: only out
+ * and the final state are written.
+ *
+ * Conventions for every entry point:
+ *  - Pointers to tensors are DEVICE pointers on the current CUDA device,
+ *    contiguous row-major, 16-byte aligned, owned by the caller.  The library
+ *    never frees or retains them past the call's completion on `stream`.
+ *  - Calls are asynchronous: they enqueue work on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream) and return once it is enqueued.
+ *  - Return value: SSM_OK (0) or a negative ssm_status; argument errors are
+ *    detected on the host before anything is enqueued.
+ *  - No CPU fallback: without a usable GPU every call fails with SSM_ERR_CUDA.
+ *  - Deterministic: identical inputs give bitwise-identical outputs.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, delta, z, out and of time-varying B, C. */
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Layout of B and C. */
+typedef enum {
+  SSM_BC_TIME_VARYING = 0, /* (batch, seqlen, dstate), io dtype, shared by all channels
+                              ("Mamba: selection": all channels share B_t and C_t) */
+  SSM_BC_PER_CHANNEL = 1   /* (dim, dstate), fp32, constant in time (an LTI system,
+                              "Recurrence and convolution") */
+} ssm_bc_layout;
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_NULL = -1,        /* a required pointer is NULL */
+  SSM_ERR_DIMS = -2,        /* batch, dim or dstate <= 0, seqlen < 0, dstate > 64,
+                               an unknown enum value, or state_in with final_state NULL */
+  SSM_ERR_ALIGN = -3,       /* a tensor pointer is not 16-byte aligned */
+  SSM_ERR_UNSUPPORTED = -4, /* a mode this build does not implement */
+  SSM_ERR_CUDA = -5,        /* a CUDA runtime error (no device, launch failure, ...) */
+  SSM_ERR_OVERLAP = -6,     /* out or final_state overlaps another tensor */
+  SSM_ERR_NOMEM = -7,       /* the workspace could not be allocated */
+  SSM_ERR_DEVICE = -8,      /* a kernel reported an internal inconsistency */
+  SSM_ERR_TIMEOUT = -9      /* a kernel gave up a bounded wait for its own copies */
+} ssm_status;
+
+typedef struct {
+  int64_t batch;          /* b  >= 1 */
+  int64_t seqlen;         /* L  >= 0; L == 0 only sets final_state (see below) */
+  int64_t dim;            /* D  >= 1, channels (d_inner) */
+  int64_t dstate;         /* N  in 1..64 */
+  int32_t io_dtype;       /* ssm_dtype */
+  int32_t bc_layout;      /* ssm_bc_layout */
+  int32_t delta_softplus; /* 1: step = softplus(delta + bias); 0: step = delta + bias */
+  int32_t state_in;       /* 1: final_state holds h_{-1} on entry (resume / recurrent step) */
+  int32_t bbar_mode;      /* 0: Bbar = step * B (the only mode built; 1 = exact ZOH is
+                             rejected with SSM_ERR_UNSUPPORTED) */
+  int32_t reserved;       /* must be 0 */
+} ssm_dims;
+
+/*
+ * Selective-scan forward.
+ *
+ *   x, delta, z, out : (batch, seqlen, dim), io dtype
+ *   A                : (dim, dstate) fp32, the diagonal of each channel's A (negative
+ *                      for a stable system; any value is accepted)
+ *   B, C             : see ssm_bc_layout
+ *   D                : (dim) fp32 skip weights, or NULL (no skip)
+ *   z                : gate input, or NULL (no gate)
+ *   delta_bias       : (dim) fp32, added before softplus, or NULL (no bias)
+ *   final_state      : (batch, dim, dstate) fp32, or NULL when state_in == 0.  On
+ *                      return (in stream order) it holds h_{L-1}; with state_in it is
+ *                      read first as h_{-1}.  With seqlen == 0 it keeps h_{-1}
+ *                      (state_in) or is zero-filled.
+ * out must not overlap any input; final_state must not overlap any other tensor.
+ * The state is accumulated in fp32 for both io dtypes; bf16 outputs are rounded to
+ * nearest even.  Long sequences are split into chunks scanned in parallel; the
+ * chunk carries live in a workspace that the library takes from its own
+ * stream-ordered memory pool on `stream` and returns to it in stream order.
+ */
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
+                           const void* B, const void* C, const float* D,
+                           const void* z, const float* delta_bias, void* out,
+                           float* final_state, const ssm_dims* dims,
+                           cudaStream_t stream);
+
+/* Waits for `stream` and returns SSM_OK, SSM_ERR_CUDA if the stream reports a CUDA
+ * error, or SSM_ERR_TIMEOUT / SSM_ERR_DEVICE if a kernel of this library raised the
+ * device status word since the last check (the word is then cleared).  Every wait
+ * inside a kernel is bounded: a copy that never lands ends the kernel with
+ * SSM_ERR_TIMEOUT instead of hanging the GPU. */
+int ssm_check_status(cudaStream_t stream);
+
+/* Static description of a status code. Never NULL. */
+const char* ssm_status_string(int code);
+
+/* Returns the unused memory of the library's per-device pools to the driver.
+ * Waits for all work on every device the library has used. */
+int ssm_release_workspace(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t ssm_kernel_launches(void);
+
+/*
+ * Tuning knobs (process-wide, for benchmarks and tests):
+ *   "chunks"        force the number of sequence chunks (0 = automatic)
+ *   "min_chunk_len" smallest automatic chunk length in steps (default 512)
+ *   "ctas_per_sm"   automatic chunking fills this many CTAs per SM (default 0: the
+ *                   kernel's occupancy)
+ *   "pow_path"      1 (default): channels whose A row is (n+1) * A[d,0] take one
+ *                   exponential per step and form the other decays as its powers;
+ *                   0: always one exponential per state
+ *   "tma"           1 (default): use the TMA-pipelined kernel where tensor maps can
+ *                   describe the tensors; 0: always the generic kernel
+ * Returns SSM_ERR_DIMS for an unknown name or a negative value.
+ */
+int ssm_set_option(const char* name, int64_t value);
+
+/*
+ * Per-kernel device timing.  While enabled, every launch is bracketed by CUDA events
+ * recorded on the launch stream.  ssm_profile_read() waits for them, writes up to
+ * `max` rows (kernel name, launches, total milliseconds) and clears the record; it
+ * returns the number of kernel kinds seen, or a negative ssm_status.
+ */
+int ssm_profile_enable(int on);
+int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

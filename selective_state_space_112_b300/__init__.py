@@ -1,5 +1,103 @@
 """B300-native (sm_103a) Mamba S6 selective-scan forward.
 
-The compute lives in a C-ABI shared library built from ``csrc/``; this
-package only marshals arguments to it.
+The compute lives in the C-ABI library ``libssmscan.so`` built from ``csrc/``
+(declarations in ``include/ssm_scan.h``).  This package only marshals PyTorch
+tensors (used for device memory and streams) into that ABI; it never computes
+any part of the scan itself and has no CPU fallback.
 """
+from __future__ import annotations
+
+from . import _abi
+from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, SSM_OK,
+                   SSMError, SsmDims)
+
+__all__ = ["ssm_selective_scan_fwd", "ssm_check_status", "ssm_status_string",
+           "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
+           "ssm_profile_enable", "ssm_profile_read", "SSMError", "SsmDims"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _addr(t):
+    return 0 if t is None else int(t.data_ptr())
+
+
+def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           out=None, final_state=None, *, delta_softplus: bool = True,
+                           state_in: bool = False, bbar_mode: int = 0,
+                           return_final_state: bool = True, stream=None):
+    """Selective-scan forward on the current CUDA device.
+
+    x, delta, z: (batch, L, dim) float32 or bfloat16 CUDA tensors, contiguous.
+    A: (dim, N) float32.  B, C: (batch, L, N) in the io dtype (time-varying,
+    shared by all channels) or (dim, N) float32 (constant per channel).
+    D, delta_bias: (dim,) float32 or None.  With ``state_in`` the initial state
+    is read from ``final_state`` (batch, dim, N) float32, which is then
+    overwritten with the final state.  Returns ``(out, final_state)``; the
+    call is asynchronous on ``stream`` (default: torch's current stream).
+    """
+    torch = _torch()
+    if x.dtype == torch.float32:
+        io = SSM_F32
+    elif x.dtype == torch.bfloat16:
+        io = SSM_BF16
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    if x.dim() != 3:
+        raise ValueError("x must be (batch, L, dim)")
+    batch, L, dim = x.shape
+    N = A.shape[-1]
+    per_channel = B.dim() == 2
+    for name, t, dt, shp in (
+            ("delta", delta, x.dtype, x.shape), ("z", z, x.dtype, x.shape),
+            ("A", A, torch.float32, (dim, N)), ("D", D, torch.float32, (dim,)),
+            ("delta_bias", delta_bias, torch.float32, (dim,)),
+            ("B", B, torch.float32 if per_channel else x.dtype, (dim, N) if per_channel else (batch, L, N)),
+            ("C", C, torch.float32 if per_channel else x.dtype, (dim, N) if per_channel else (batch, L, N))):
+        if t is None:
+            continue
+        if t.dtype != dt or tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{name}: expected {dt} {tuple(shp)}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and (state_in or return_final_state):
+        if state_in:
+            raise ValueError("state_in needs final_state holding the initial state")
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device)
+    dims = SsmDims(batch=batch, seqlen=L, dim=dim, dstate=N, io_dtype=io,
+                   bc_layout=SSM_BC_PER_CHANNEL if per_channel else SSM_BC_TIME_VARYING,
+                   delta_softplus=int(bool(delta_softplus)), state_in=int(bool(state_in)),
+                   bbar_mode=int(bbar_mode), reserved=0)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = _abi.call_fwd(_addr(x), _addr(delta), _addr(A), _addr(B), _addr(C), _addr(D),
+                       _addr(z), _addr(delta_bias), _addr(out), _addr(final_state), dims,
+                       int(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_selective_scan_fwd")
+    return out, final_state
+
+
+def ssm_check_status(stream=None) -> int:
+    if stream is None:
+        stream = _torch().cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    return _abi.check_status(int(stream))
+
+
+ssm_status_string = _abi.status_string
+ssm_release_workspace = _abi.release_workspace
+ssm_kernel_launches = _abi.kernel_launches
+ssm_set_option = _abi.set_option
+ssm_profile_enable = _abi.profile_enable
+ssm_profile_read = _abi.profile_read

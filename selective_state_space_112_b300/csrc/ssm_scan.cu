@@ -1,0 +1,453 @@
+// C ABI of the selective-scan forward (declared in include/ssm_scan.h): argument
+// checks, chunk planning, tensor maps, the stream-ordered workspace pool and
+// kernel dispatch.
+#include "ssm_scan.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "scan_kernels.cuh"
+
+namespace {
+
+using ssm::ScanParams;
+
+// ----------------------------------------------------------------- options
+
+std::atomic<int64_t> g_opt_chunks{0};
+std::atomic<int64_t> g_opt_min_chunk_len{512};
+std::atomic<int64_t> g_opt_ctas_per_sm{0};
+std::atomic<int64_t> g_opt_pow_path{1};
+std::atomic<int64_t> g_opt_tma{1};
+std::atomic<uint64_t> g_launches{0};
+
+__device__ int g_status;  // raised by a kernel: kStatusTimeout, or any other nonzero value
+
+// ------------------------------------------------------------- profiling
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+const char* const kKindName[2] = {"ssm_chunk_aggregate", "ssm_scan_output"};
+
+// ------------------------------------------------------- per-device pools
+
+std::mutex g_pool_mu;
+std::vector<cudaMemPool_t> g_pools;  // index = device ordinal; nullptr = not created
+
+cudaError_t get_pool(int dev, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if ((int)g_pools.size() <= dev) g_pools.resize(dev + 1, nullptr);
+  if (!g_pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse: no allocation in steady state
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return e;
+    g_pools[dev] = pool;
+  }
+  *out = g_pools[dev];
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- planning
+
+struct Plan {
+  int npt, tpc;
+  bool tma;  // fast kernel (tensor maps) or generic kernel
+  int nchunks;
+  int64_t chunk_len;
+};
+
+void bucket(int64_t N, int* npt, int* tpc) {
+  if (N <= 4) { *npt = 4; *tpc = 1; }
+  else if (N <= 8) { *npt = 8; *tpc = 1; }
+  else if (N <= 16) { *npt = 16; *tpc = 1; }
+  else if (N <= 32) { *npt = 16; *tpc = 2; }
+  else { *npt = 16; *tpc = 4; }
+}
+
+// A tensor map needs 16-byte row pitches: the channel row of x / delta / z and, for
+// time-varying B / C, the state row.
+bool tma_ok(const ssm_dims& d) {
+  const int64_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
+  if ((d.dim * esz) % 16) return false;
+  if (d.bc_layout == SSM_BC_TIME_VARYING && (d.dstate * esz) % 16) return false;
+  if (d.seqlen >= (1ll << 31) || d.dim >= (1ll << 31) || d.batch >= (1ll << 31)) return false;
+  return true;
+}
+
+// ----------------------------------------------------------------- dispatch
+
+typedef void (*GenericFn)(ScanParams);
+typedef void (*TmaFn)(ssm::TmaMaps, ScanParams);
+
+struct Kernel {
+  GenericFn generic = nullptr;
+  TmaFn tma = nullptr;
+  int smem = 0;  // dynamic shared memory of the fast kernel
+  const void* fn() const { return tma ? (const void*)tma : (const void*)generic; }
+};
+
+template <typename IO, int NPT, int TPC, bool LTI, int PASS>
+Kernel make_kernel(bool tma) {
+  Kernel k;
+  if (tma) {
+    k.tma = ssm::scan_tma_kernel<IO, NPT, TPC, LTI, PASS>;
+    k.smem = ssm::tma_smem_bytes<IO, NPT, TPC>();
+  } else {
+    k.generic = ssm::scan_generic_kernel<IO, NPT, TPC, LTI, PASS>;
+  }
+  return k;
+}
+
+template <typename IO, bool LTI, int PASS>
+Kernel pick3(int npt, int tpc, bool tma) {
+  if (npt == 4) return make_kernel<IO, 4, 1, LTI, PASS>(tma);
+  if (npt == 8) return make_kernel<IO, 8, 1, LTI, PASS>(tma);
+  if (tpc == 1) return make_kernel<IO, 16, 1, LTI, PASS>(tma);
+  if (tpc == 2) return make_kernel<IO, 16, 2, LTI, PASS>(tma);
+  return make_kernel<IO, 16, 4, LTI, PASS>(tma);
+}
+
+Kernel kernel_for(int io, bool lti, int pass, int npt, int tpc, bool tma) {
+  if (io == SSM_F32) {
+    if (lti) return pass ? pick3<ssm::F32, true, 1>(npt, tpc, tma) : pick3<ssm::F32, true, 0>(npt, tpc, tma);
+    return pass ? pick3<ssm::F32, false, 1>(npt, tpc, tma) : pick3<ssm::F32, false, 0>(npt, tpc, tma);
+  }
+  if (lti) return pass ? pick3<ssm::BF16, true, 1>(npt, tpc, tma) : pick3<ssm::BF16, true, 0>(npt, tpc, tma);
+  return pass ? pick3<ssm::BF16, false, 1>(npt, tpc, tma) : pick3<ssm::BF16, false, 0>(npt, tpc, tma);
+}
+
+// Resident CTAs per SM of a kernel (cached), after raising its shared-memory limit.
+int occupancy(const Kernel& k) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& e : cache)
+    if (e.first == k.fn()) return e.second;
+  if (k.smem > 48 * 1024)
+    cudaFuncSetAttribute(k.fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.fn(), ssm::kThreads, k.smem) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  cache.push_back({k.fn(), occ});
+  return occ;
+}
+
+Plan make_plan(const ssm_dims& d, int sm_count) {
+  Plan pl;
+  bucket(d.dstate, &pl.npt, &pl.tpc);
+  pl.tma = g_opt_tma.load() && tma_ok(d);
+  const bool lti = d.bc_layout == SSM_BC_PER_CHANNEL;
+  const int occ = g_opt_ctas_per_sm.load() > 0
+                      ? (int)g_opt_ctas_per_sm.load()
+                      : occupancy(kernel_for(d.io_dtype, lti, 1, pl.npt, pl.tpc, pl.tma));
+  const int64_t ch_per_cta = ssm::kThreads / pl.tpc;
+  const int64_t ctas = d.batch * ((d.dim + ch_per_cta - 1) / ch_per_cta);
+  int64_t k = g_opt_chunks.load();
+  if (k <= 0) {
+    // as many chunks as fill one wave of resident CTAs, no more (a partial second
+    // wave would double the time); chunks no shorter than min_chunk_len
+    const int64_t slots = (int64_t)sm_count * occ;
+    k = std::max<int64_t>(1, slots / ctas);
+    const int64_t min_len = std::max<int64_t>(ssm::kTB, g_opt_min_chunk_len.load());
+    k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / min_len));
+  }
+  k = std::max<int64_t>(1, std::min<int64_t>(k, (d.seqlen + ssm::kTB - 1) / ssm::kTB));
+  k = std::min<int64_t>(k, 65535);
+  // chunk length: a multiple of 32 steps, so tiles and blocks never straddle chunks
+  int64_t len = (d.seqlen + k - 1) / k;
+  len = ((len + ssm::kTB - 1) / ssm::kTB) * ssm::kTB;
+  pl.chunk_len = std::max<int64_t>(len, ssm::kTB);
+  pl.nchunks = (int)((d.seqlen + pl.chunk_len - 1) / pl.chunk_len);
+  return pl;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a row-major (batch, rows, inner) tensor with a box of (inner_box, rows_box, 1).
+bool encode3d(CUtensorMap* m, const void* base, int esz, int64_t inner, int64_t rows, int64_t batch,
+              int inner_box, int rows_box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)(inner * esz), (cuuint64_t)(inner * rows * esz)};
+  const cuuint32_t box[3] = {(cuuint32_t)inner_box, (cuuint32_t)rows_box, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch(const Kernel& kn, int kind, dim3 grid, const ssm::TmaMaps* maps, const ScanParams& p,
+           cudaStream_t stream) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaEventRecord(e0, stream) != cudaSuccess) return SSM_ERR_CUDA;
+  }
+  if (kn.tma) {
+    occupancy(kn);  // sets the shared-memory attribute on first use
+    kn.tma<<<grid, ssm::kThreads, kn.smem, stream>>>(*maps, p);
+  } else {
+    kn.generic<<<grid, ssm::kThreads, 0, stream>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return SSM_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (prof) {
+    if (cudaEventRecord(e1, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({kind, e0, e1});
+  }
+  return SSM_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_status_string(int code) {
+  switch (code) {
+    case SSM_OK: return "ok";
+    case SSM_ERR_NULL: return "a required pointer is NULL";
+    case SSM_ERR_DIMS: return "invalid sizes or flags";
+    case SSM_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case SSM_ERR_UNSUPPORTED: return "mode not implemented in this build";
+    case SSM_ERR_CUDA: return "CUDA runtime error";
+    case SSM_ERR_OVERLAP: return "an output overlaps another tensor";
+    case SSM_ERR_NOMEM: return "workspace allocation failed";
+    case SSM_ERR_DEVICE: return "a kernel reported an internal inconsistency";
+    case SSM_ERR_TIMEOUT: return "a kernel gave up waiting for its copies";
+    default: return "unknown status";
+  }
+}
+
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, void* out, float* final_state,
+                           const ssm_dims* dims, cudaStream_t stream) {
+  if (!dims) return SSM_ERR_NULL;
+  const ssm_dims d = *dims;
+  if (d.batch <= 0 || d.dim <= 0 || d.dstate <= 0 || d.dstate > 64 || d.seqlen < 0)
+    return SSM_ERR_DIMS;
+  if ((d.io_dtype != SSM_F32 && d.io_dtype != SSM_BF16) ||
+      (d.bc_layout != SSM_BC_TIME_VARYING && d.bc_layout != SSM_BC_PER_CHANNEL) ||
+      (d.delta_softplus != 0 && d.delta_softplus != 1) || (d.state_in != 0 && d.state_in != 1) ||
+      (d.bbar_mode != 0 && d.bbar_mode != 1) || d.reserved != 0)
+    return SSM_ERR_DIMS;
+  if (d.state_in && !final_state) return SSM_ERR_DIMS;
+  if (d.bbar_mode == 1) return SSM_ERR_UNSUPPORTED;
+  if (d.seqlen > 0 && (!x || !delta || !A || !B || !C || !out)) return SSM_ERR_NULL;
+  const void* ptrs[] = {x, delta, A, B, C, D, z, delta_bias, out, final_state};
+  for (const void* q : ptrs)
+    if (q && ((uintptr_t)q & 15u)) return SSM_ERR_ALIGN;
+
+  const size_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
+  const size_t act = (size_t)d.batch * d.seqlen * d.dim * esz;
+  const bool lti = d.bc_layout == SSM_BC_PER_CHANNEL;
+  const size_t bc = lti ? (size_t)d.dim * d.dstate * 4 : (size_t)d.batch * d.seqlen * d.dstate * esz;
+  const size_t st = (size_t)d.batch * d.dim * d.dstate * 4;
+  struct { const void* p; size_t n; } ins[] = {
+      {x, act}, {delta, act}, {A, (size_t)d.dim * d.dstate * 4}, {B, bc}, {C, bc},
+      {D, (size_t)d.dim * 4}, {z, act}, {delta_bias, (size_t)d.dim * 4}};
+  for (auto& in : ins) {
+    if (overlaps(out, act, in.p, in.n)) return SSM_ERR_OVERLAP;
+    if (overlaps(final_state, st, in.p, in.n)) return SSM_ERR_OVERLAP;
+  }
+  if (overlaps(final_state, st, out, act)) return SSM_ERR_OVERLAP;
+
+  if (d.seqlen == 0) {
+    if (final_state && !d.state_in &&
+        cudaMemsetAsync(final_state, 0, st, stream) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (d.batch > 65535) return SSM_ERR_DIMS;
+  const Plan pl = make_plan(d, sms);
+
+  ScanParams p;
+  std::memset(&p, 0, sizeof p);
+  p.x = x; p.delta = delta; p.z = z; p.out = out; p.A = A; p.B = B; p.C = C;
+  p.Dskip = D; p.bias = delta_bias; p.final_state = final_state;
+  p.h_init = d.state_in ? final_state : nullptr;
+  p.batch = d.batch; p.seqlen = d.seqlen; p.dim = d.dim; p.dstate = (int)d.dstate;
+  p.nchunks = pl.nchunks; p.chunk_len = pl.chunk_len;
+  p.delta_softplus = d.delta_softplus;
+  p.pow_path = (int)g_opt_pow_path.load();
+  int* status = nullptr;
+  if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
+  p.status = status;
+
+  const int64_t ch_per_cta = ssm::kThreads / pl.tpc;
+  const unsigned gx = (unsigned)((d.dim + ch_per_cta - 1) / ch_per_cta);
+
+  ssm::TmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (pl.tma) {
+    const int T = d.io_dtype == SSM_BF16 ? ssm::TileSteps<ssm::BF16>::value : ssm::TileSteps<ssm::F32>::value;
+    const int ebytes = (int)esz;
+    bool okm = encode3d(&maps.x, x, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T) &&
+               encode3d(&maps.delta, delta, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T);
+    if (okm && z) okm = encode3d(&maps.z, z, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T);
+    if (okm && !lti)
+      okm = encode3d(&maps.B, B, ebytes, d.dstate, d.seqlen, d.batch, (int)d.dstate, T) &&
+            encode3d(&maps.C, C, ebytes, d.dstate, d.seqlen, d.batch, (int)d.dstate, T);
+    if (!okm) return SSM_ERR_CUDA;
+  }
+
+  void* ws = nullptr;
+  if (pl.nchunks > 1) {
+    const size_t nH = (size_t)(pl.nchunks - 1) * d.batch * d.dim * d.dstate;
+    const size_t nS = (size_t)(pl.nchunks - 1) * d.batch * d.dim;
+    const size_t nh0 = d.state_in ? (size_t)d.batch * d.dim * d.dstate : 0;
+    const size_t bytes = (nH + nS + nh0) * sizeof(float);
+    cudaMemPool_t pool;
+    if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+    p.ws_H = static_cast<float*>(ws);
+    p.ws_S = p.ws_H + nH;
+    p.ws_h0 = nh0 ? p.ws_S + nS : nullptr;
+    int rc = launch(kernel_for(d.io_dtype, lti, 0, pl.npt, pl.tpc, pl.tma), 0,
+                    dim3(gx, (unsigned)(pl.nchunks - 1), (unsigned)d.batch), &maps, p, stream);
+    if (rc != SSM_OK) {
+      cudaFreeAsync(ws, stream);
+      return rc;
+    }
+  }
+  int rc = launch(kernel_for(d.io_dtype, lti, 1, pl.npt, pl.tpc, pl.tma), 1,
+                  dim3(gx, (unsigned)pl.nchunks, (unsigned)d.batch), &maps, p, stream);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
+  return rc;
+}
+
+int ssm_check_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SSM_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) return SSM_ERR_CUDA;
+  if (v == 0) return SSM_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return SSM_ERR_CUDA;
+  return v == ssm::kStatusTimeout ? SSM_ERR_TIMEOUT : SSM_ERR_DEVICE;
+}
+
+int ssm_release_workspace(void) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return SSM_ERR_CUDA;
+  int rc = SSM_OK;
+  for (int dev = 0; dev < (int)g_pools.size(); ++dev) {
+    if (!g_pools[dev]) continue;
+    if (cudaSetDevice(dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemPoolTrimTo(g_pools[dev], 0) != cudaSuccess)
+      rc = SSM_ERR_CUDA;
+  }
+  cudaSetDevice(cur);
+  return rc;
+}
+
+uint64_t ssm_kernel_launches(void) { return g_launches.load(); }
+
+int ssm_set_option(const char* name, int64_t value) {
+  if (!name || value < 0) return SSM_ERR_DIMS;
+  if (!std::strcmp(name, "chunks")) g_opt_chunks = value;
+  else if (!std::strcmp(name, "min_chunk_len")) g_opt_min_chunk_len = value;
+  else if (!std::strcmp(name, "ctas_per_sm")) g_opt_ctas_per_sm = value;
+  else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
+  else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;
+  else return SSM_ERR_DIMS;
+  return SSM_OK;
+}
+
+int ssm_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return SSM_OK;
+}
+
+int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, int max) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  int64_t cnt[2] = {0, 0};
+  double ms[2] = {0, 0};
+  int rc = SSM_OK;
+  for (auto& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      rc = SSM_ERR_CUDA;
+    cnt[r.kind] += 1;
+    ms[r.kind] += t;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  if (rc != SSM_OK) return rc;
+  int rows = 0;
+  for (int k = 0; k < 2; ++k) {
+    if (!cnt[k]) continue;
+    if (rows < max) {
+      if (names) names[rows] = kKindName[k];
+      if (launches) launches[rows] = cnt[k];
+      if (total_ms) total_ms[rows] = ms[k];
+    }
+    ++rows;
+  }
+  return rows;
+}
+
+}  // extern "C"

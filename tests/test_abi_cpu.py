@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/ssm_scan.h declares, and rejects bad arguments on the host
+before touching the device."""
+import os
+import re
+
+import pytest
+
+from selective_state_space_112_b300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert set(names) == set(_abi.EXPORTS), names
+    L = _abi.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    for code in list(_abi.STATUS) + [-99]:
+        s = _abi.status_string(code)
+        assert isinstance(s, str) and s
+    assert _abi.status_string(0) == "ok"
+
+
+def dims(**kw):
+    base = dict(batch=2, seqlen=16, dim=8, dstate=4, io_dtype=0, bc_layout=0,
+                delta_softplus=1, state_in=0, bbar_mode=0, reserved=0)
+    base.update(kw)
+    return _abi.SsmDims(**base)
+
+
+# Fake, never dereferenced device addresses: validation happens first on the host.
+BASE = 1 << 40
+P = {k: BASE + i * (1 << 30) for i, k in enumerate(
+    ["x", "delta", "A", "B", "C", "D", "z", "bias", "out", "fs"])}
+
+
+def call(d, **over):
+    q = dict(P)
+    q.update(over)
+    return _abi.call_fwd(q["x"], q["delta"], q["A"], q["B"], q["C"], q["D"], q["z"],
+                         q["bias"], q["out"], q["fs"], d, 0)
+
+
+def test_null_dims():
+    L = _abi.lib()
+    assert L.ssm_selective_scan_fwd(*([None] * 10), None, None) == -1
+
+
+@pytest.mark.parametrize("bad", [dict(batch=0), dict(dim=0), dict(dstate=0), dict(dstate=65),
+                                 dict(seqlen=-1), dict(io_dtype=2), dict(bc_layout=3),
+                                 dict(delta_softplus=2), dict(state_in=5), dict(reserved=1),
+                                 dict(bbar_mode=9)])
+def test_bad_dims(bad):
+    assert call(dims(**bad)) == -2
+
+
+def test_state_in_needs_state():
+    assert call(dims(state_in=1), fs=0) == -2
+
+
+def test_null_required_pointer():
+    for k in ("x", "delta", "A", "B", "C", "out"):
+        assert call(dims(), **{k: 0}) == -1, k
+
+
+def test_misaligned():
+    for k in ("x", "delta", "A", "B", "C", "D", "z", "bias", "out", "fs"):
+        assert call(dims(), **{k: P[k] + 4}) == -3, k
+
+
+def test_overlap():
+    assert call(dims(), out=P["x"] + 16) == -6
+    assert call(dims(), fs=P["out"]) == -6
+    assert call(dims(), fs=P["A"]) == -6
+
+
+def test_exact_zoh_not_built():
+    assert call(dims(bbar_mode=1)) == -4
+
+
+def test_no_cpu_fallback():
+    """A valid call without a usable GPU must fail, never compute on the host."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call(dims()) == -5
+
+
+def test_options():
+    with pytest.raises(_abi.SSMError):
+        _abi.set_option("no_such_option", 1)
+    with pytest.raises(_abi.SSMError):
+        _abi.set_option("chunks", -1)
+    for name in ("chunks", "min_chunk_len", "ctas_per_sm"):
+        _abi.set_option(name, 0)
+    _abi.set_option("min_chunk_len", 512)
+    _abi.set_option("pow_path", 1)
+    _abi.set_option("tma", 1)
+    assert _abi.profile_read() == {}

@@ -1,0 +1,244 @@
+"""Parity of the CUDA path (through the C ABI) against the float64 oracle.
+
+Bars: floored max relative error <= 1e-5 for fp32 inputs and <= 2e-2 for bf16
+inputs (out compared in its stored dtype against the unrounded oracle; the fp32
+final state compared the same way).  Small cases compare every element; the
+full-size Mamba-shaped workloads compare every output of sampled channels,
+which the oracle scans over their whole length, in the launch configuration
+the benchmark times.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.metrics import TOL, floored_rel_err
+from selective_state_space_112_b300.workloads import config, make_workload
+
+from helpers import assert_close, device_inputs, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _options():
+    import selective_state_space_112_b300 as ssm
+    defaults = dict(chunks=0, pow_path=1, tma=1)
+    for k, v in defaults.items():
+        ssm.ssm_set_option(k, v)
+    yield
+    for k, v in defaults.items():
+        ssm.ssm_set_option(k, v)
+
+
+def full_check(w, what=""):
+    g_out, g_fs = run_gpu(w)
+    r_out, r_fs = run_oracle(w)
+    assert_close(g_out, r_out, w.io, f"{what} out")
+    assert_close(g_fs, r_fs, w.io, f"{what} final_state")
+    return g_out, g_fs, r_out, r_fs
+
+
+# ------------------------------------------------------------ the six workloads
+
+def test_tiny_f32():
+    full_check(config("tiny_f32"), "tiny_f32")
+
+
+def test_lti_f32_and_convolution():
+    """LTI workload: parity with the oracle's scan and with the causal
+    convolution by K_k = C Abar^k Bbar (plus D x)."""
+    w = config("lti_f32")
+    g_out, _, _, _ = full_check(w, "lti_f32")
+    dt = w.delta[0, 0, :].astype(np.float64)
+    K = oracle.lti_kernel(w.A, w.B, w.C, dt, w.seqlen)
+    conv = oracle.causal_conv(w.x, K, w.D)
+    assert floored_rel_err(g_out, conv) <= TOL["f32"]
+
+
+def test_mamba130m_f32_full():
+    full_check(config("mamba130m_f32"), "mamba130m_f32")
+
+
+def sampled_check(w, nsample, seed):
+    """Run the GPU on the full workload; the oracle scans sampled channels."""
+    rng = np.random.default_rng(seed)
+    picks = sorted({(int(rng.integers(w.batch)), int(rng.integers(w.dim))) for _ in range(nsample)})
+    picks += [(0, 0), (w.batch - 1, w.dim - 1)]
+    g_out, g_fs = run_gpu(w)
+    ref = oracle.selective_scan_channels(picks, w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
+                                         delta_bias=w.delta_bias, h0=w.h0,
+                                         delta_softplus=w.delta_softplus, io_dtype=w.io)
+    go = np.stack([g_out[b, :, d] for b, d in ref])
+    ro = np.stack([ref[k][0] for k in ref])
+    gs = np.stack([g_fs[b, d] for b, d in ref])
+    rs = np.stack([ref[k][1] for k in ref])
+    assert_close(go, ro, w.io, f"{w.name} sampled out")
+    assert_close(gs, rs, w.io, f"{w.name} sampled final_state")
+    assert np.all(np.isfinite(g_out)) and np.all(np.isfinite(g_fs))
+    return g_out, g_fs
+
+
+def test_mamba1p4b_bf16_sampled():
+    sampled_check(config("mamba1p4b_bf16"), 96, 3)
+
+
+def test_long_bf16_sampled():
+    """L = 131072: many chunks; the carry crosses every chunk boundary."""
+    sampled_check(config("long_bf16"), 48, 4)
+
+
+def test_step_bf16_full():
+    """Recurrent step: L = 1 with a stored state, every output and state checked."""
+    full_check(config("step_bf16"), "step_bf16")
+
+
+# ------------------------------------------------------------------ edge cases
+
+EDGE = [
+    # (name, make_workload kwargs, forced chunk count)
+    ("L1", dict(batch=2, seqlen=1, dim=40, dstate=16), 0),
+    ("ragged_L", dict(batch=2, seqlen=77, dim=136, dstate=16), 0),
+    ("ragged_L_chunks3", dict(batch=2, seqlen=100, dim=136, dstate=16), 3),
+    ("chunks7_state_in", dict(batch=3, seqlen=333, dim=72, dstate=16, state_in=True), 7),
+    ("many_chunks", dict(batch=1, seqlen=4000, dim=256, dstate=16), 125),
+    ("ragged_D_generic", dict(batch=2, seqlen=90, dim=130, dstate=16), 2),
+    ("N1", dict(batch=2, seqlen=65, dim=33, dstate=1), 2),
+    ("N3", dict(batch=2, seqlen=65, dim=33, dstate=3), 2),
+    ("N4", dict(batch=2, seqlen=65, dim=64, dstate=4), 2),
+    ("N8", dict(batch=2, seqlen=129, dim=200, dstate=8), 3),
+    ("N13", dict(batch=2, seqlen=96, dim=64, dstate=13), 2),
+    ("N17", dict(batch=2, seqlen=96, dim=64, dstate=17), 2),
+    ("N32", dict(batch=2, seqlen=96, dim=72, dstate=32), 3),
+    ("N64", dict(batch=1, seqlen=96, dim=72, dstate=64, state_in=True), 2),
+    ("no_gate_no_D_no_bias", dict(batch=2, seqlen=90, dim=48, dstate=16, gate=False,
+                                  with_D=False, with_bias=False), 2),
+    ("s4d_real_pow", dict(batch=2, seqlen=300, dim=96, dstate=16, a_init="s4d_real"), 2),
+    ("lti", dict(batch=2, seqlen=200, dim=40, dstate=16, lti=True, with_bias=False,
+                 a_init="random"), 3),
+    ("D5", dict(batch=4, seqlen=33, dim=5, dstate=4), 0),
+]
+
+
+@pytest.mark.parametrize("tma", [1, 0])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("name,kw,chunks", EDGE, ids=[e[0] for e in EDGE])
+def test_edge(name, kw, chunks, io, tma):
+    """Both kernels (TMA-pipelined where a tensor map fits, and the generic one)."""
+    import selective_state_space_112_b300 as ssm
+    ssm.ssm_set_option("chunks", chunks)
+    ssm.ssm_set_option("tma", tma)
+    w = make_workload(name, io=io, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    full_check(w, f"{name}/{io}/tma{tma}")
+
+
+def test_pow_and_generic_paths_agree_with_oracle():
+    """S4D-real A takes the powers path; with it disabled, the one-exponential-per-
+    state path must match the oracle too.  A mixed-A batch with a wider spread of
+    A (long-memory channels with step * |A| down to ~1e-5) exercises both."""
+    import selective_state_space_112_b300 as ssm
+    for io in ("f32", "bf16"):
+        w = make_workload("s4d", batch=2, seqlen=500, dim=256, dstate=16, a_init="s4d_real",
+                          seed=7, io=io)
+        full_check(w, f"pow on {io}")
+        ssm.ssm_set_option("pow_path", 0)
+        full_check(w, f"pow off {io}")
+        ssm.ssm_set_option("pow_path", 1)
+        w.A[::3] = -np.exp(np.random.default_rng(1).normal(0, 0.7, size=w.A[::3].shape)).astype(np.float32)
+        full_check(w, f"mixed A {io}")
+
+
+def test_deterministic_bitwise():
+    w = make_workload("det", batch=2, seqlen=3000, dim=304, dstate=16, io="bf16", seed=9)
+    dev = device_inputs(w)
+    a = run_gpu(w, dev)
+    b = run_gpu(w, dev)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_split_resume_matches_single_call():
+    """Final state as checkpoint: scan(L1) then scan(L2) from it == scan(L1 + L2)."""
+    import torch
+    import selective_state_space_112_b300 as ssm
+    w = make_workload("split", batch=2, seqlen=1500, dim=200, dstate=16, seed=12)
+    dev = device_inputs(w)
+    out_full, fs_full = ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"],
+                                                   dev["C"], dev["D"], dev["z"], dev["delta_bias"])
+    cut = 611
+    s1, s2 = slice(0, cut), slice(cut, None)
+    part = lambda t, s: t[:, s].contiguous()
+    o1, f1 = ssm.ssm_selective_scan_fwd(part(dev["x"], s1), part(dev["delta"], s1), dev["A"],
+                                        part(dev["B"], s1), part(dev["C"], s1), dev["D"],
+                                        part(dev["z"], s1), dev["delta_bias"])
+    o2, f2 = ssm.ssm_selective_scan_fwd(part(dev["x"], s2), part(dev["delta"], s2), dev["A"],
+                                        part(dev["B"], s2), part(dev["C"], s2), dev["D"],
+                                        part(dev["z"], s2), dev["delta_bias"], final_state=f1,
+                                        state_in=True)
+    torch.cuda.synchronize()
+    got = torch.cat([o1, o2], dim=1).double().cpu().numpy()
+    assert floored_rel_err(got, out_full.double().cpu().numpy()) <= TOL["f32"]
+    assert floored_rel_err(f2.cpu().numpy(), fs_full.cpu().numpy()) <= TOL["f32"]
+
+
+def test_step_calls_equal_scan():
+    """k recurrent single-step calls == one scan of length k."""
+    import torch
+    import selective_state_space_112_b300 as ssm
+    w = make_workload("steps", batch=3, seqlen=24, dim=64, dstate=16, io="bf16", seed=13)
+    dev = device_inputs(w)
+    out_full, fs_full = ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"],
+                                                   dev["C"], dev["D"], dev["z"], dev["delta_bias"])
+    fs = torch.zeros_like(fs_full)
+    outs = []
+    for t in range(w.seqlen):
+        s = slice(t, t + 1)
+        o, fs = ssm.ssm_selective_scan_fwd(dev["x"][:, s].contiguous(), dev["delta"][:, s].contiguous(),
+                                           dev["A"], dev["B"][:, s].contiguous(),
+                                           dev["C"][:, s].contiguous(), dev["D"],
+                                           dev["z"][:, s].contiguous(), dev["delta_bias"],
+                                           final_state=fs, state_in=True)
+        outs.append(o)
+    torch.cuda.synchronize()
+    got = torch.cat(outs, dim=1).float().cpu().numpy()
+    assert floored_rel_err(got, out_full.float().cpu().numpy()) <= 1e-2  # bf16 output rounding
+    assert floored_rel_err(fs.cpu().numpy(), fs_full.cpu().numpy()) <= 1e-5
+
+
+def test_zero_length():
+    import torch
+    import selective_state_space_112_b300 as ssm
+    w = make_workload("L0", batch=2, seqlen=0, dim=16, dstate=4, state_in=True, seed=1)
+    dev = device_inputs(w)
+    fs = dev["final_state"].clone()
+    _, f = ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
+                                      dev["D"], dev["z"], dev["delta_bias"], final_state=fs,
+                                      state_in=True)
+    torch.cuda.synchronize()
+    assert torch.equal(f, dev["final_state"])
+    f2 = torch.full_like(fs, 7.0)
+    _, f2 = ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
+                                       final_state=f2)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(f2).item() == 0
+
+
+def test_device_errors_are_reported():
+    import torch
+    import selective_state_space_112_b300 as ssm
+    w = make_workload("err", batch=1, seqlen=8, dim=16, dstate=4, seed=2)
+    dev = device_inputs(w)
+    big = torch.empty(1 + w.x.size, dtype=torch.float32, device="cuda")
+    mis = big[1:].view(w.x.shape)                      # 4-byte offset: misaligned
+    with pytest.raises(ssm.SSMError) as e:
+        ssm.ssm_selective_scan_fwd(mis, dev["delta"], dev["A"], dev["B"], dev["C"])
+    assert e.value.code == -3
+    with pytest.raises(ssm.SSMError) as e:
+        ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
+                                   out=dev["x"])
+    assert e.value.code == -6
+    with pytest.raises(ssm.SSMError) as e:
+        ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
+                                   bbar_mode=1)
+    assert e.value.code == -4
+    assert ssm.ssm_check_status() == 0
