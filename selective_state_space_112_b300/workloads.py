@@ -144,7 +144,8 @@ def make_workload(name: str, batch: int, seqlen: int, dim: int, dstate: int, *,
 
 
 # The five scan workloads and the recurrent-step workload (sizes from the
-# Mamba-shaped layers they stand for).
+# Mamba-shaped layers they stand for), plus a shortened long-context case for
+# profiler captures.
 CONFIGS = {
     "tiny_f32": dict(batch=1, seqlen=256, dim=16, dstate=4, io="f32", seed=0,
                      a_init="random", gate=True),
@@ -158,6 +159,10 @@ CONFIGS = {
                       a_init="random", gate=True),
     "step_bf16": dict(batch=256, seqlen=1, dim=2560, dstate=16, io="bf16", seed=5,
                       a_init="random", gate=True, state_in=True),
+    # the long-context layer cut to 16384 steps (inputs 252 MB, still larger than L2):
+    # the size used for full profiler captures, which replay each launch ~40 times
+    "long_bf16_16k": dict(batch=1, seqlen=16384, dim=2560, dstate=16, io="bf16", seed=4,
+                          a_init="random", gate=True),
 }
 
 
