@@ -125,8 +125,15 @@ uint64_t ssm_kernel_launches(void);
  * Tuning knobs (process-wide, for benchmarks and tests):
  *   "chunks"        force the number of sequence chunks (0 = automatic)
  *   "min_chunk_len" smallest automatic chunk length in steps (default 512)
- *   "ctas_per_sm"   automatic chunking fills this many CTAs per SM (default 0: the
- *                   kernel's occupancy)
+ *   "lanes"         force the lanes per channel G (1, 2 or 4; 0 = automatic).
+ *                   Each channel's states are split over G threads.  A G the build
+ *                   lacks for this state count makes calls fail with
+ *                   SSM_ERR_UNSUPPORTED.
+ *   "lane_threads"  automatic G: the fewest lanes giving batch * dim * G >= this
+ *                   (default 32768); G = 1 when no G reaches it
+ *   "ctas_per_sm"   automatic chunking: cut the sequence only when the channels give
+ *                   fewer than this many CTAs per SM (default 3); the chunk count then
+ *                   fills that many CTAs per SM in one wave
  *   "pow_path"      1 (default): channels whose A row is (n+1) * A[d,0] take one
  *                   exponential per step and form the other decays as its powers;
  *                   0: always one exponential per state

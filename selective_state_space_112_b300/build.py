@@ -1,22 +1,27 @@
 """Build the selective-scan C-ABI library (libssmscan.so) for sm_103a with nvcc.
 
-The library is built in-tree next to this file; the CUDA runtime is linked
-statically, so the .so depends only on the NVIDIA driver.
+The kernel instantiations are spread over several translation units, compiled in
+parallel into object files under _build/ and linked into libssmscan.so next to
+this file.  The CUDA runtime is linked statically, so the .so depends only on the
+NVIDIA driver.
 """
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SRC = [os.path.join(HERE, "csrc", "ssm_scan.cu")]
-DEPS = SRC + [os.path.join(HERE, "csrc", "scan_kernels.cuh"),
-              os.path.join(ROOT, "include", "ssm_scan.h")]
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libssmscan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "-I", os.path.join(ROOT, "include")]
 
 
 def nvcc() -> str:
@@ -26,17 +31,37 @@ def nvcc() -> str:
     return cand
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in DEPS)):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-           "-I", os.path.join(ROOT, "include"), "-o", tmp, *SRC]
+def sources():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def headers():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "ssm_scan.h")]
+
+
+def _compile(src: str, verbose: bool) -> str:
+    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, "-c", "-o", obj, src]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    if verbose:
+        sys.stderr.write(r.stdout + r.stderr)
+    return obj
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    deps = sources() + headers()
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in deps)):
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    with ThreadPoolExecutor(max_workers=max(1, min(len(sources()), os.cpu_count() or 1))) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose), sources()))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -1,0 +1,59 @@
+// Kernel lookup for the tiled selective-scan kernel: one entry per (io dtype, B/C
+// layout, pass, states per lane S, lanes per channel G).  The instantiations are
+// spread over four translation units (kernels_<io>_<layout>.cu) so that they build
+// in parallel.
+#pragma once
+
+#include "scan_tile.cuh"
+
+namespace ssm {
+
+typedef void (*TileFn)(TmaMaps, ScanParams);
+
+struct KernelInfo {
+  TileFn fn = nullptr;
+  int nt = 0;    // threads per CTA
+  int ch = 0;    // channels per CTA
+  int t = 0;     // steps per tile
+  int smem = 0;  // dynamic shared memory bytes
+};
+
+// (S, G) pairs built: S states per lane in {2, 4, 8, 16}, G lanes per channel in
+// {1, 2, 4}, S * G (the padded state count) in {2, ..., 64}.
+#define SSM_FOR_EACH_SG(X) \
+  X(2, 1) X(4, 1) X(2, 2) X(8, 1) X(4, 2) X(2, 4) X(16, 1) X(8, 2) X(4, 4) \
+  X(16, 2) X(8, 4) X(16, 4)
+
+template <typename IO, int S, int G, bool LTI, int PASS>
+KernelInfo kernel_info() {
+  using Gm = Geo<IO, S, G>;
+  KernelInfo k;
+  k.fn = scan_tile_kernel<IO, S, G, LTI, PASS>;
+  k.nt = Gm::NT;
+  k.ch = Gm::CH;
+  k.t = Gm::T;
+  k.smem = Gm::BYTES;
+  return k;
+}
+
+template <typename IO, bool LTI, int PASS>
+KernelInfo pick_sg(int S, int G) {
+#define SSM_CASE(s_, g_) \
+  if (S == s_ && G == g_) return kernel_info<IO, s_, g_, LTI, PASS>();
+  SSM_FOR_EACH_SG(SSM_CASE)
+#undef SSM_CASE
+  return KernelInfo();
+}
+
+template <typename IO, bool LTI>
+KernelInfo lookup_impl(int S, int G, int pass) {
+  return pass ? pick_sg<IO, LTI, 1>(S, G) : pick_sg<IO, LTI, 0>(S, G);
+}
+
+// Defined in kernels_<io>_<layout>.cu.
+KernelInfo lookup_f32_tv(int S, int G, int pass);
+KernelInfo lookup_f32_lti(int S, int G, int pass);
+KernelInfo lookup_bf16_tv(int S, int G, int pass);
+KernelInfo lookup_bf16_lti(int S, int G, int pass);
+
+}  // namespace ssm

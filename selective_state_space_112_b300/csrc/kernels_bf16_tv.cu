@@ -1,0 +1,6 @@
+// Instantiations of the tiled selective-scan kernel: bf16 inputs, time-varying B and C.
+#include "kernel_table.cuh"
+
+namespace ssm {
+KernelInfo lookup_bf16_tv(int S, int G, int pass) { return lookup_impl<BF16, false>(S, G, pass); }
+}  // namespace ssm

@@ -15,7 +15,7 @@
 #include <utility>
 #include <vector>
 
-#include "scan_kernels.cuh"
+#include "kernel_table.cuh"
 
 namespace {
 
@@ -25,7 +25,9 @@ using ssm::ScanParams;
 
 std::atomic<int64_t> g_opt_chunks{0};
 std::atomic<int64_t> g_opt_min_chunk_len{512};
-std::atomic<int64_t> g_opt_ctas_per_sm{0};
+std::atomic<int64_t> g_opt_lanes{0};
+std::atomic<int64_t> g_opt_lane_threads{32768};
+std::atomic<int64_t> g_opt_ctas_per_sm{3};
 std::atomic<int64_t> g_opt_pow_path{1};
 std::atomic<int64_t> g_opt_tma{1};
 std::atomic<uint64_t> g_launches{0};
@@ -73,116 +75,126 @@ cudaError_t get_pool(int dev, cudaMemPool_t* out) {
 // ---------------------------------------------------------------- planning
 
 struct Plan {
-  int npt, tpc;
-  bool tma;  // fast kernel (tensor maps) or generic kernel
-  int nchunks;
-  int64_t chunk_len;
+  int S = 0, G = 0;      // states per lane, lanes per channel
+  bool tma = false;      // TMA-pipelined tiles (else the generic global-memory path)
+  int nchunks = 1;
+  int64_t chunk_len = 0;
+  ssm::KernelInfo out_k, agg_k;
 };
 
-void bucket(int64_t N, int* npt, int* tpc) {
-  if (N <= 4) { *npt = 4; *tpc = 1; }
-  else if (N <= 8) { *npt = 8; *tpc = 1; }
-  else if (N <= 16) { *npt = 16; *tpc = 1; }
-  else if (N <= 32) { *npt = 16; *tpc = 2; }
-  else { *npt = 16; *tpc = 4; }
+ssm::KernelInfo lookup(int io, bool lti, int S, int G, int pass) {
+  if (io == SSM_F32) return lti ? ssm::lookup_f32_lti(S, G, pass) : ssm::lookup_f32_tv(S, G, pass);
+  return lti ? ssm::lookup_bf16_lti(S, G, pass) : ssm::lookup_bf16_tv(S, G, pass);
+}
+
+// Padded state count: the next power of two >= max(N, 2).
+int padded_states(int64_t N) {
+  int ns = 2;
+  while (ns < N) ns *= 2;
+  return ns;
 }
 
 // A tensor map needs 16-byte row pitches: the channel row of x / delta / z and, for
-// time-varying B / C, the state row.
+// time-varying B / C, the state row, which must also fill the kernel's padded row
+// (N a power of two).
 bool tma_ok(const ssm_dims& d) {
   const int64_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
   if ((d.dim * esz) % 16) return false;
-  if (d.bc_layout == SSM_BC_TIME_VARYING && (d.dstate * esz) % 16) return false;
+  if (d.bc_layout == SSM_BC_TIME_VARYING &&
+      ((d.dstate * esz) % 16 || padded_states(d.dstate) != d.dstate))
+    return false;
   if (d.seqlen >= (1ll << 31) || d.dim >= (1ll << 31) || d.batch >= (1ll << 31)) return false;
   return true;
 }
 
-// ----------------------------------------------------------------- dispatch
-
-typedef void (*GenericFn)(ScanParams);
-typedef void (*TmaFn)(ssm::TmaMaps, ScanParams);
-
-struct Kernel {
-  GenericFn generic = nullptr;
-  TmaFn tma = nullptr;
-  int smem = 0;  // dynamic shared memory of the fast kernel
-  const void* fn() const { return tma ? (const void*)tma : (const void*)generic; }
-};
-
-template <typename IO, int NPT, int TPC, bool LTI, int PASS>
-Kernel make_kernel(bool tma) {
-  Kernel k;
-  if (tma) {
-    k.tma = ssm::scan_tma_kernel<IO, NPT, TPC, LTI, PASS>;
-    k.smem = ssm::tma_smem_bytes<IO, NPT, TPC>();
-  } else {
-    k.generic = ssm::scan_generic_kernel<IO, NPT, TPC, LTI, PASS>;
-  }
-  return k;
+// Sets the kernel's shared-memory limit once (it may exceed the 48 KB default).
+bool prepare(const ssm::KernelInfo& k) {
+  static std::mutex mu;
+  static std::vector<const void*> done;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto f : done)
+    if (f == (const void*)k.fn) return true;
+  if (cudaFuncSetAttribute((const void*)k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
+      cudaSuccess)
+    return false;
+  done.push_back((const void*)k.fn);
+  return true;
 }
 
-template <typename IO, bool LTI, int PASS>
-Kernel pick3(int npt, int tpc, bool tma) {
-  if (npt == 4) return make_kernel<IO, 4, 1, LTI, PASS>(tma);
-  if (npt == 8) return make_kernel<IO, 8, 1, LTI, PASS>(tma);
-  if (tpc == 1) return make_kernel<IO, 16, 1, LTI, PASS>(tma);
-  if (tpc == 2) return make_kernel<IO, 16, 2, LTI, PASS>(tma);
-  return make_kernel<IO, 16, 4, LTI, PASS>(tma);
-}
-
-Kernel kernel_for(int io, bool lti, int pass, int npt, int tpc, bool tma) {
-  if (io == SSM_F32) {
-    if (lti) return pass ? pick3<ssm::F32, true, 1>(npt, tpc, tma) : pick3<ssm::F32, true, 0>(npt, tpc, tma);
-    return pass ? pick3<ssm::F32, false, 1>(npt, tpc, tma) : pick3<ssm::F32, false, 0>(npt, tpc, tma);
-  }
-  if (lti) return pass ? pick3<ssm::BF16, true, 1>(npt, tpc, tma) : pick3<ssm::BF16, true, 0>(npt, tpc, tma);
-  return pass ? pick3<ssm::BF16, false, 1>(npt, tpc, tma) : pick3<ssm::BF16, false, 0>(npt, tpc, tma);
-}
-
-// Resident CTAs per SM of a kernel (cached), after raising its shared-memory limit.
-int occupancy(const Kernel& k) {
+// Resident CTAs per SM of a kernel (cached).
+int occupancy(const ssm::KernelInfo& k) {
   static std::mutex mu;
   static std::vector<std::pair<const void*, int>> cache;
-  std::lock_guard<std::mutex> lk(mu);
-  for (auto& e : cache)
-    if (e.first == k.fn()) return e.second;
-  if (k.smem > 48 * 1024)
-    cudaFuncSetAttribute(k.fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& e : cache)
+      if (e.first == (const void*)k.fn) return e.second;
+  }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.fn(), ssm::kThreads, k.smem) != cudaSuccess ||
+  if (!prepare(k) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)k.fn, k.nt, k.smem) != cudaSuccess ||
       occ < 1)
     occ = 1;
-  cache.push_back({k.fn(), occ});
+  std::lock_guard<std::mutex> lk(mu);
+  cache.push_back({(const void*)k.fn, occ});
   return occ;
 }
 
-Plan make_plan(const ssm_dims& d, int sm_count) {
-  Plan pl;
-  bucket(d.dstate, &pl.npt, &pl.tpc);
-  pl.tma = g_opt_tma.load() && tma_ok(d);
+// Lanes per channel: the fewest (least per-state overhead) that give at least
+// `lane_threads` threads over the batch rows and channels; one otherwise (the
+// sequence is then chunked).
+// Chunks along the sequence only when that leaves fewer than `ctas_per_sm` CTAs per
+// SM: every chunk but the last is then scanned twice (aggregate, output), so the
+// chunk count is the largest that still fits ctas_per_sm CTAs on every SM (one
+// wave, evenly spread).
+bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
+  const int ns = padded_states(d.dstate);
   const bool lti = d.bc_layout == SSM_BC_PER_CHANNEL;
-  const int occ = g_opt_ctas_per_sm.load() > 0
-                      ? (int)g_opt_ctas_per_sm.load()
-                      : occupancy(kernel_for(d.io_dtype, lti, 1, pl.npt, pl.tpc, pl.tma));
-  const int64_t ch_per_cta = ssm::kThreads / pl.tpc;
-  const int64_t ctas = d.batch * ((d.dim + ch_per_cta - 1) / ch_per_cta);
+  std::vector<int> cand;
+  for (int G = 1; G <= 4; G *= 2) {
+    const int S = ns / G;
+    if (S >= 2 && S <= 16 && lookup(d.io_dtype, lti, S, G, 1).fn) cand.push_back(G);
+  }
+  if (cand.empty()) return false;
+  const int64_t forced = g_opt_lanes.load();
+  int G = 0;
+  if (forced > 0) {
+    for (int c : cand)
+      if (c == forced) G = c;
+    if (!G) return false;
+  } else {
+    // the fewest lanes that reach lane_threads; if even the most cannot, the sequence
+    // must be chunked anyway, and one lane per channel (least per-state work) is best
+    G = cand.front();
+    for (int c : cand)
+      if (d.batch * d.dim * c >= g_opt_lane_threads.load()) {
+        G = c;
+        break;
+      }
+  }
+  pl->G = G;
+  pl->S = ns / G;
+  pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1);
+  pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0);
+  pl->tma = g_opt_tma.load() && tma_ok(d);
   int64_t k = g_opt_chunks.load();
   if (k <= 0) {
-    // as many chunks as fill one wave of resident CTAs, no more (a partial second
-    // wave would double the time); chunks no shorter than min_chunk_len
-    const int64_t slots = (int64_t)sm_count * occ;
-    k = std::max<int64_t>(1, slots / ctas);
-    const int64_t min_len = std::max<int64_t>(ssm::kTB, g_opt_min_chunk_len.load());
+    const int64_t ctas = d.batch * ((d.dim + pl->out_k.ch - 1) / pl->out_k.ch);
+    const int64_t per_sm = std::max<int64_t>(
+        1, std::min<int64_t>(g_opt_ctas_per_sm.load(), occupancy(pl->out_k)));
+    const int64_t want = (int64_t)sms * per_sm;
+    k = ctas >= want ? 1 : std::max<int64_t>(1, want / ctas);
+    const int64_t min_len = std::max<int64_t>(ssm::kChunkAlign, g_opt_min_chunk_len.load());
     k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / min_len));
   }
-  k = std::max<int64_t>(1, std::min<int64_t>(k, (d.seqlen + ssm::kTB - 1) / ssm::kTB));
+  k = std::max<int64_t>(1, std::min<int64_t>(k, (d.seqlen + ssm::kChunkAlign - 1) / ssm::kChunkAlign));
   k = std::min<int64_t>(k, 65535);
-  // chunk length: a multiple of 32 steps, so tiles and blocks never straddle chunks
+  // chunk length: a multiple of kChunkAlign steps, so tiles never straddle chunks
   int64_t len = (d.seqlen + k - 1) / k;
-  len = ((len + ssm::kTB - 1) / ssm::kTB) * ssm::kTB;
-  pl.chunk_len = std::max<int64_t>(len, ssm::kTB);
-  pl.nchunks = (int)((d.seqlen + pl.chunk_len - 1) / pl.chunk_len);
-  return pl;
+  len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
+  pl->chunk_len = std::max<int64_t>(len, ssm::kChunkAlign);
+  pl->nchunks = (int)((d.seqlen + pl->chunk_len - 1) / pl->chunk_len);
+  return true;
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -216,8 +228,9 @@ bool encode3d(CUtensorMap* m, const void* base, int esz, int64_t inner, int64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch(const Kernel& kn, int kind, dim3 grid, const ssm::TmaMaps* maps, const ScanParams& p,
+int launch(const ssm::KernelInfo& kn, int kind, dim3 grid, const ssm::TmaMaps& maps, const ScanParams& p,
            cudaStream_t stream) {
+  if (!kn.fn || !prepare(kn)) return SSM_ERR_CUDA;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   bool prof;
   {
@@ -228,12 +241,7 @@ int launch(const Kernel& kn, int kind, dim3 grid, const ssm::TmaMaps* maps, cons
     if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return SSM_ERR_CUDA;
     if (cudaEventRecord(e0, stream) != cudaSuccess) return SSM_ERR_CUDA;
   }
-  if (kn.tma) {
-    occupancy(kn);  // sets the shared-memory attribute on first use
-    kn.tma<<<grid, ssm::kThreads, kn.smem, stream>>>(*maps, p);
-  } else {
-    kn.generic<<<grid, ssm::kThreads, 0, stream>>>(p);
-  }
+  kn.fn<<<grid, kn.nt, kn.smem, stream>>>(maps, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return SSM_ERR_CUDA;
   g_launches.fetch_add(1);
@@ -314,10 +322,10 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SSM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SSM_ERR_CUDA;
   if (d.batch > 65535) return SSM_ERR_DIMS;
-  const Plan pl = make_plan(d, sms);
+  Plan pl;
+  if (!make_plan(d, sms, &pl)) return SSM_ERR_UNSUPPORTED;
 
   ScanParams p;
   std::memset(&p, 0, sizeof p);
@@ -328,24 +336,24 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
   p.nchunks = pl.nchunks; p.chunk_len = pl.chunk_len;
   p.delta_softplus = d.delta_softplus;
   p.pow_path = (int)g_opt_pow_path.load();
+  p.use_tma = pl.tma ? 1 : 0;
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
   p.status = status;
 
-  const int64_t ch_per_cta = ssm::kThreads / pl.tpc;
-  const unsigned gx = (unsigned)((d.dim + ch_per_cta - 1) / ch_per_cta);
+  const int ch = pl.out_k.ch, T = pl.out_k.t;
+  const unsigned gx = (unsigned)((d.dim + ch - 1) / ch);
 
   ssm::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
   if (pl.tma) {
-    const int T = d.io_dtype == SSM_BF16 ? ssm::TileSteps<ssm::BF16>::value : ssm::TileSteps<ssm::F32>::value;
-    const int ebytes = (int)esz;
-    bool okm = encode3d(&maps.x, x, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T) &&
-               encode3d(&maps.delta, delta, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T);
-    if (okm && z) okm = encode3d(&maps.z, z, ebytes, d.dim, d.seqlen, d.batch, (int)ch_per_cta, T);
+    const int eb = (int)esz;
+    bool okm = encode3d(&maps.x, x, eb, d.dim, d.seqlen, d.batch, ch, T) &&
+               encode3d(&maps.delta, delta, eb, d.dim, d.seqlen, d.batch, ch, T);
+    if (okm && z) okm = encode3d(&maps.z, z, eb, d.dim, d.seqlen, d.batch, ch, T);
     if (okm && !lti)
-      okm = encode3d(&maps.B, B, ebytes, d.dstate, d.seqlen, d.batch, (int)d.dstate, T) &&
-            encode3d(&maps.C, C, ebytes, d.dstate, d.seqlen, d.batch, (int)d.dstate, T);
+      okm = encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T) &&
+            encode3d(&maps.C, C, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T);
     if (!okm) return SSM_ERR_CUDA;
   }
 
@@ -361,15 +369,13 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
     p.ws_H = static_cast<float*>(ws);
     p.ws_S = p.ws_H + nH;
     p.ws_h0 = nh0 ? p.ws_S + nS : nullptr;
-    int rc = launch(kernel_for(d.io_dtype, lti, 0, pl.npt, pl.tpc, pl.tma), 0,
-                    dim3(gx, (unsigned)(pl.nchunks - 1), (unsigned)d.batch), &maps, p, stream);
+    int rc = launch(pl.agg_k, 0, dim3(gx, (unsigned)(pl.nchunks - 1), (unsigned)d.batch), maps, p, stream);
     if (rc != SSM_OK) {
       cudaFreeAsync(ws, stream);
       return rc;
     }
   }
-  int rc = launch(kernel_for(d.io_dtype, lti, 1, pl.npt, pl.tpc, pl.tma), 1,
-                  dim3(gx, (unsigned)pl.nchunks, (unsigned)d.batch), &maps, p, stream);
+  int rc = launch(pl.out_k, 1, dim3(gx, (unsigned)pl.nchunks, (unsigned)d.batch), maps, p, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
   return rc;
 }
@@ -405,6 +411,8 @@ int ssm_set_option(const char* name, int64_t value) {
   if (!name || value < 0) return SSM_ERR_DIMS;
   if (!std::strcmp(name, "chunks")) g_opt_chunks = value;
   else if (!std::strcmp(name, "min_chunk_len")) g_opt_min_chunk_len = value;
+  else if (!std::strcmp(name, "lanes")) g_opt_lanes = value;
+  else if (!std::strcmp(name, "lane_threads")) g_opt_lane_threads = value;
   else if (!std::strcmp(name, "ctas_per_sm")) g_opt_ctas_per_sm = value;
   else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
   else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;

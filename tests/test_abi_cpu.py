@@ -103,9 +103,11 @@ def test_options():
         _abi.set_option("no_such_option", 1)
     with pytest.raises(_abi.SSMError):
         _abi.set_option("chunks", -1)
-    for name in ("chunks", "min_chunk_len", "ctas_per_sm"):
+    for name in ("chunks", "min_chunk_len", "lanes"):
         _abi.set_option(name, 0)
     _abi.set_option("min_chunk_len", 512)
+    _abi.set_option("lane_threads", 36864)
+    _abi.set_option("ctas_per_sm", 2)
     _abi.set_option("pow_path", 1)
     _abi.set_option("tma", 1)
     assert _abi.profile_read() == {}

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _options():
     import selective_state_space_112_b300 as ssm
-    defaults = dict(chunks=0, pow_path=1, tma=1)
+    defaults = dict(chunks=0, pow_path=1, tma=1, lanes=0)
     for k, v in defaults.items():
         ssm.ssm_set_option(k, v)
     yield
@@ -131,6 +131,38 @@ def test_edge(name, kw, chunks, io, tma):
     ssm.ssm_set_option("tma", tma)
     w = make_workload(name, io=io, seed=zlib.crc32(name.encode()) % 1000, **kw)
     full_check(w, f"{name}/{io}/tma{tma}")
+
+
+LANE_CASES = [
+    # (name, make_workload kwargs, forced chunk count)
+    ("N16", dict(batch=2, seqlen=300, dim=72, dstate=16), 3),
+    ("N16_ragged_state_in", dict(batch=1, seqlen=77, dim=40, dstate=16, state_in=True), 0),
+    ("N4", dict(batch=2, seqlen=65, dim=48, dstate=4), 2),
+    ("N8", dict(batch=2, seqlen=129, dim=64, dstate=8), 0),
+    ("N13", dict(batch=2, seqlen=70, dim=24, dstate=13), 2),
+    ("N32", dict(batch=1, seqlen=96, dim=40, dstate=32), 2),
+    ("N64", dict(batch=1, seqlen=50, dim=24, dstate=64, state_in=True), 2),
+    ("lti16", dict(batch=2, seqlen=200, dim=40, dstate=16, lti=True, with_bias=False), 3),
+    ("s4d16", dict(batch=2, seqlen=200, dim=40, dstate=16, a_init="s4d_real"), 2),
+]
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 4])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("name,kw,chunks", LANE_CASES, ids=[c[0] for c in LANE_CASES])
+def test_lanes_per_channel(name, kw, chunks, io, lanes):
+    """Every split of a channel's states over G lanes (S = padded N / G states per
+    lane, 2 <= S <= 16) against the oracle, with and without sequence chunks."""
+    import selective_state_space_112_b300 as ssm
+    ns = 2
+    while ns < kw["dstate"]:
+        ns *= 2
+    if not 2 <= ns // lanes <= 16:
+        pytest.skip(f"no kernel with {lanes} lanes for N={kw['dstate']}")
+    ssm.ssm_set_option("lanes", lanes)
+    ssm.ssm_set_option("chunks", chunks)
+    w = make_workload(name, io=io, seed=zlib.crc32((name + io).encode()) % 1000, **kw)
+    full_check(w, f"{name}/{io}/G{lanes}")
 
 
 def test_pow_and_generic_paths_agree_with_oracle():
