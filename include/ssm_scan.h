@@ -61,7 +61,9 @@ typedef enum {
   SSM_ERR_OVERLAP = -6,     /* out or final_state overlaps another tensor */
   SSM_ERR_NOMEM = -7,       /* the workspace could not be allocated */
   SSM_ERR_DEVICE = -8,      /* a kernel reported an internal inconsistency */
-  SSM_ERR_TIMEOUT = -9      /* a kernel gave up a bounded wait for its own copies */
+  SSM_ERR_TIMEOUT = -9,     /* a kernel gave up a bounded wait for its own copies */
+  SSM_ERR_SCRATCH = -10     /* ssm_selective_scan_fwd_noalloc: the call needs more than
+                               SSM_NOALLOC_SCRATCH_BYTES of workspace */
 } ssm_status;
 
 typedef struct {
@@ -103,6 +105,37 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
                            const void* z, const float* delta_bias, void* out,
                            float* final_state, const ssm_dims* dims,
                            cudaStream_t stream);
+
+/* Bytes of the fixed workspace of ssm_selective_scan_fwd_noalloc (16 MiB). */
+#define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Selective-scan forward that allocates no device memory.
+ *
+ * The source pages have no counterpart to this entry point: it exists for callers that
+ * cannot let a library allocate device memory (an application whose arena owns all
+ * device memory, a serving loop that allows no allocation after warm-up, an allocator
+ * that must not be entered from the calling thread).  Arguments, layouts, results and
+ * errors are those of ssm_selective_scan_fwd, with these differences:
+ *  - The chunk-carry workspace lives in one fixed device array of
+ *    SSM_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that loads it
+ *    until the process exits.  A call whose workspace would be larger (long sequences
+ *    with many chunks: (chunks - 1) * batch * dim * (dstate + 1) * 4 bytes, plus
+ *    batch * dim * dstate * 4 with state_in) returns SSM_ERR_SCRATCH and launches
+ *    nothing.  Calls that need no chunking use no workspace.
+ *  - The first call on a device asks the runtime for the array's address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the array and the array keeps the last call's
+ *    contents (nothing in it must start at zero).  Calls that may overlap on the GPU
+ *    (different streams without ordering) race on it: order them on one stream.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int ssm_selective_scan_fwd_noalloc(const void* x, const void* delta, const float* A,
+                                   const void* B, const void* C, const float* D,
+                                   const void* z, const float* delta_bias, void* out,
+                                   float* final_state, const ssm_dims* dims,
+                                   cudaStream_t stream);
 
 /* Waits for `stream` and returns SSM_OK, SSM_ERR_CUDA if the stream reports a CUDA
  * error, or SSM_ERR_TIMEOUT / SSM_ERR_DEVICE if a kernel of this library raised the

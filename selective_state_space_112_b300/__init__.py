@@ -11,7 +11,7 @@ from . import _abi
 from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, SSM_OK,
                    SSMError, SsmDims)
 
-__all__ = ["ssm_selective_scan_fwd", "ssm_check_status", "ssm_status_string",
+__all__ = ["ssm_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc", "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read", "SSMError", "SsmDims"]
 
@@ -28,7 +28,7 @@ def _addr(t):
 def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                            out=None, final_state=None, *, delta_softplus: bool = True,
                            state_in: bool = False, bbar_mode: int = 0,
-                           return_final_state: bool = True, stream=None):
+                           return_final_state: bool = True, stream=None, _noalloc: bool = False):
     """Selective-scan forward on the current CUDA device.
 
     x, delta, z: (batch, L, dim) float32 or bfloat16 CUDA tensors, contiguous.
@@ -81,10 +81,24 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         stream = stream.cuda_stream
     rc = _abi.call_fwd(_addr(x), _addr(delta), _addr(A), _addr(B), _addr(C), _addr(D),
                        _addr(z), _addr(delta_bias), _addr(out), _addr(final_state), dims,
-                       int(stream))
+                       int(stream), noalloc=_noalloc)
     if rc != SSM_OK:
-        raise SSMError(rc, "ssm_selective_scan_fwd")
+        raise SSMError(rc, "ssm_selective_scan_fwd_noalloc" if _noalloc else "ssm_selective_scan_fwd")
     return out, final_state
+
+
+def ssm_selective_scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                                   out=None, final_state=None, **kw):
+    """Same call as ``ssm_selective_scan_fwd`` through the library entry point that
+    allocates no device memory for its own work: the chunk-carry workspace sits in a
+    fixed 16 MiB device array inside the library (shared by all such calls on a device,
+    so calls that overlap on the GPU race), and problems that need more raise SSMError
+    with code SSM_ERR_SCRATCH.  It is meant for callers that cannot let a library
+    allocate.  ``out`` and ``final_state`` should be passed in by such callers; when
+    they are omitted, this binding creates them with torch, as the other entry point
+    does."""
+    return ssm_selective_scan_fwd(x, delta, A, B, C, D, z, delta_bias, out, final_state,
+                                  _noalloc=True, **kw)
 
 
 def ssm_check_status(stream=None) -> int:

@@ -19,10 +19,13 @@ STATUS = {
     0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_DIMS", -3: "SSM_ERR_ALIGN",
     -4: "SSM_ERR_UNSUPPORTED", -5: "SSM_ERR_CUDA", -6: "SSM_ERR_OVERLAP",
     -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_DEVICE", -9: "SSM_ERR_TIMEOUT",
+    -10: "SSM_ERR_SCRATCH",
 }
 SSM_OK = 0
+SSM_ERR_SCRATCH = -10
+SSM_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/ssm_scan.h
 # names as declared in include/ssm_scan.h
-EXPORTS = ("ssm_selective_scan_fwd", "ssm_check_status", "ssm_status_string",
+EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc", "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read")
 
@@ -61,6 +64,8 @@ def lib():
             vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             L.ssm_selective_scan_fwd.restype = i32
             L.ssm_selective_scan_fwd.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
+            L.ssm_selective_scan_fwd_noalloc.restype = i32
+            L.ssm_selective_scan_fwd_noalloc.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_check_status.restype = i32
             L.ssm_check_status.argtypes = [vp]
             L.ssm_status_string.restype = ctypes.c_char_p
@@ -86,13 +91,13 @@ def status_string(code: int) -> str:
 
 
 def call_fwd(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims: SsmDims,
-             stream) -> int:
-    """Raw call: every tensor argument is an integer address (0 = NULL)."""
-    return lib().ssm_selective_scan_fwd(x or None, delta or None, A or None, B or None,
-                                        C or None, D or None, z or None,
-                                        delta_bias or None, out or None,
-                                        final_state or None, ctypes.byref(dims),
-                                        stream or None)
+             stream, noalloc: bool = False) -> int:
+    """Raw call: every tensor argument is an integer address (0 = NULL).  With
+    ``noalloc`` the call goes to ssm_selective_scan_fwd_noalloc."""
+    fn = lib().ssm_selective_scan_fwd_noalloc if noalloc else lib().ssm_selective_scan_fwd
+    return fn(x or None, delta or None, A or None, B or None, C or None, D or None,
+              z or None, delta_bias or None, out or None, final_state or None,
+              ctypes.byref(dims), stream or None)
 
 
 def check_status(stream=0) -> int:

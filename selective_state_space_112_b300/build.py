@@ -36,7 +36,8 @@ def sources():
 
 
 def headers():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "ssm_scan.h")]
+    return (sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")))
+            + [os.path.join(ROOT, "include", "ssm_scan.h")])
 
 
 def _compile(src: str, verbose: bool) -> str:

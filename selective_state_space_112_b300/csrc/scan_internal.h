@@ -1,0 +1,18 @@
+// Library-internal entry shared by the public C entry points of libssmscan.
+#pragma once
+
+#include <stddef.h>
+
+#include "ssm_scan.h"
+
+namespace ssm_internal {
+
+// Runs one selective-scan call.  With scratch == nullptr the chunk-carry workspace
+// comes from the library's memory pool; otherwise it is taken from the caller's
+// scratch_bytes of device memory at `scratch` and nothing is allocated.
+int scan_forward(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, void* out,
+                 float* final_state, const ssm_dims* dims, cudaStream_t stream, void* scratch,
+                 size_t scratch_bytes);
+
+}  // namespace ssm_internal

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "kernel_table.cuh"
+#include "scan_internal.h"
 
 namespace {
 
@@ -275,14 +276,23 @@ const char* ssm_status_string(int code) {
     case SSM_ERR_NOMEM: return "workspace allocation failed";
     case SSM_ERR_DEVICE: return "a kernel reported an internal inconsistency";
     case SSM_ERR_TIMEOUT: return "a kernel gave up waiting for its copies";
+    case SSM_ERR_SCRATCH: return "the call needs more scratch than the fixed no-allocation buffer holds";
     default: return "unknown status";
   }
 }
 
-int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
-                           const void* C, const float* D, const void* z,
-                           const float* delta_bias, void* out, float* final_state,
-                           const ssm_dims* dims, cudaStream_t stream) {
+}  // extern "C"
+
+namespace ssm_internal {
+
+// The whole call.  scratch == nullptr: the chunk-carry workspace comes from the
+// library's stream-ordered pool.  Otherwise it is carved from `scratch`
+// (scratch_bytes long, device memory the caller keeps), nothing is allocated, and a
+// call whose workspace does not fit returns SSM_ERR_SCRATCH before launching.
+int scan_forward(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, void* out,
+                 float* final_state, const ssm_dims* dims, cudaStream_t stream, void* scratch,
+                 size_t scratch_bytes) {
   if (!dims) return SSM_ERR_NULL;
   const ssm_dims d = *dims;
   if (d.batch <= 0 || d.dim <= 0 || d.dstate <= 0 || d.dstate > 64 || d.seqlen < 0)
@@ -363,21 +373,38 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
     const size_t nS = (size_t)(pl.nchunks - 1) * d.batch * d.dim;
     const size_t nh0 = d.state_in ? (size_t)d.batch * d.dim * d.dstate : 0;
     const size_t bytes = (nH + nS + nh0) * sizeof(float);
-    cudaMemPool_t pool;
-    if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
-    if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
-    p.ws_H = static_cast<float*>(ws);
+    if (scratch) {
+      if (bytes > scratch_bytes) return SSM_ERR_SCRATCH;
+      p.ws_H = static_cast<float*>(scratch);
+    } else {
+      cudaMemPool_t pool;
+      if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+      if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+      p.ws_H = static_cast<float*>(ws);
+    }
     p.ws_S = p.ws_H + nH;
     p.ws_h0 = nh0 ? p.ws_S + nS : nullptr;
     int rc = launch(pl.agg_k, 0, dim3(gx, (unsigned)(pl.nchunks - 1), (unsigned)d.batch), maps, p, stream);
     if (rc != SSM_OK) {
-      cudaFreeAsync(ws, stream);
+      if (ws) cudaFreeAsync(ws, stream);
       return rc;
     }
   }
   int rc = launch(pl.out_k, 1, dim3(gx, (unsigned)pl.nchunks, (unsigned)d.batch), maps, p, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
   return rc;
+}
+
+}  // namespace ssm_internal
+
+extern "C" {
+
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, void* out, float* final_state,
+                           const ssm_dims* dims, cudaStream_t stream) {
+  return ssm_internal::scan_forward(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims, stream,
+                                    nullptr, 0);
 }
 
 int ssm_check_status(cudaStream_t stream) {
