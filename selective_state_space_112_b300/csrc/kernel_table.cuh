@@ -56,4 +56,8 @@ KernelInfo lookup_f32_lti(int S, int G, int pass);
 KernelInfo lookup_bf16_tv(int S, int G, int pass);
 KernelInfo lookup_bf16_lti(int S, int G, int pass);
 
+// Recurrent step kernel (sequence length 1), step_kernel.cu: G threads per channel of
+// 4 states each, G in {1, 2, 4, 8, 16}.
+KernelInfo lookup_step(int io_bf16, bool lti, int G);
+
 }  // namespace ssm

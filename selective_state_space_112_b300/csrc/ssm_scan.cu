@@ -44,7 +44,7 @@ struct ProfRec {
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof;
-const char* const kKindName[2] = {"ssm_chunk_aggregate", "ssm_scan_output"};
+const char* const kKindName[3] = {"ssm_chunk_aggregate", "ssm_scan_output", "ssm_step"};
 
 // ------------------------------------------------------- per-device pools
 
@@ -332,6 +332,27 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+
+  if (d.seqlen == 1) {
+    // recurrent step: one pass over the state, no tiles, no chunks, no workspace
+    int ns = 4;
+    while (ns < d.dstate) ns *= 2;
+    const int G = ns / 4;
+    const ssm::KernelInfo k = ssm::lookup_step(d.io_dtype == SSM_BF16, lti, G);
+    ScanParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x; p.delta = delta; p.z = z; p.out = out; p.A = A; p.B = B; p.C = C;
+    p.Dskip = D; p.bias = delta_bias; p.final_state = final_state;
+    p.h_init = d.state_in ? final_state : nullptr;
+    p.batch = d.batch; p.seqlen = 1; p.dim = d.dim; p.dstate = (int)d.dstate;
+    p.nchunks = 1; p.chunk_len = 1;
+    p.delta_softplus = d.delta_softplus;
+    ssm::TmaMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    const int64_t threads = d.batch * d.dim * G;
+    if ((threads + k.nt - 1) / k.nt > INT32_MAX) return SSM_ERR_DIMS;
+    return launch(k, 2, dim3((unsigned)((threads + k.nt - 1) / k.nt)), maps, p, stream);
+  }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SSM_ERR_CUDA;
   if (d.batch > 65535) return SSM_ERR_DIMS;
   Plan pl;
@@ -459,8 +480,8 @@ int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, in
     std::lock_guard<std::mutex> lk(g_prof_mu);
     recs.swap(g_prof);
   }
-  int64_t cnt[2] = {0, 0};
-  double ms[2] = {0, 0};
+  int64_t cnt[3] = {0, 0, 0};
+  double ms[3] = {0, 0, 0};
   int rc = SSM_OK;
   for (auto& r : recs) {
     float t = 0.f;
@@ -473,7 +494,7 @@ int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, in
   }
   if (rc != SSM_OK) return rc;
   int rows = 0;
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 3; ++k) {
     if (!cnt[k]) continue;
     if (rows < max) {
       if (names) names[rows] = kKindName[k];
