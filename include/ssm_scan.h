@@ -162,8 +162,9 @@ uint64_t ssm_kernel_launches(void);
  *                   Each channel's states are split over G threads.  A G the build
  *                   lacks for this state count makes calls fail with
  *                   SSM_ERR_UNSUPPORTED.
- *   "lane_threads"  automatic G: the fewest lanes giving batch * dim * G >= this
- *                   (default 32768); G = 1 when no G reaches it
+ *   "lane_threads"  automatic G for bf16 inputs: the fewest lanes giving
+ *                   batch * dim * G >= this (default 32768); G = 1 when no G reaches
+ *                   it.  fp32 inputs use G = 1.
  *   "ctas_per_sm"   automatic chunking: cut the sequence only when the channels give
  *                   fewer than this many CTAs per SM (default 3); the chunk count then
  *                   fills that many CTAs per SM in one wave

@@ -22,7 +22,7 @@
 //    per-(step, channel) work is repeated and nothing round-trips through shared
 //    memory.
 //  * Each CTA has four consumer warps and one producer warp.  The producer fills a
-//    4-stage ring of input tiles (x, delta, z: T steps x CH channels; B, C: T x N)
+//    3- or 4-stage ring of input tiles (x, delta, z: T steps x CH channels; B, C: T x N)
 //    with TMA (cp.async.bulk.tensor), or with plain loads for shapes a tensor map
 //    cannot describe, completed on "full" mbarriers; consumer warps release a stage
 //    on its "empty" mbarrier.  There is no CTA-wide barrier in the main loop: warps
@@ -273,8 +273,9 @@ struct Geo {
   static constexpr int CH = NW * CW;               // channels per CTA
   static constexpr int NS = S * G;                 // padded state count (>= N)
   static constexpr int ESZ = IO::kBytes;
-  static constexpr int T = (CH * ESZ <= 256) ? 16 : 8;   // steps per tile
-  static constexpr int ST = 3;                     // stages
+  // steps per tile: the longest of 32 / 16 / 8 whose x / delta / z tiles fit 12 KB
+  static constexpr int T = (3 * 32 * CH * ESZ <= 12288) ? 32 : (3 * 16 * CH * ESZ <= 12288) ? 16 : 8;
+  static constexpr int ST = (G == 1) ? 3 : 4;     // stages (fewer: more CTAs per SM)
   static constexpr int al(int v) { return (v + 127) / 128 * 128; }
   static constexpr int XB = al(T * CH * ESZ);      // one x / delta / z tile
   static constexpr int BB = al(T * NS * ESZ);      // one raw B / C tile (io dtype)
@@ -670,7 +671,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   //   A  this lane's step of each round: step size, u (and the S4D-real base)
   //   B  the G R steps in order: shuffled step sizes, state updates, C . h shares
   //   C  reduce-scatter of the shares, D x, gate, store
-  constexpr int R = (T / G >= 8) ? 8 : T / G;
+  constexpr int R = (G == 1) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
   auto run = [&](auto pow_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value && !LTI;

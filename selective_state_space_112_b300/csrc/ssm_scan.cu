@@ -163,6 +163,10 @@ bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
     for (int c : cand)
       if (c == forced) G = c;
     if (!G) return false;
+  } else if (d.io_dtype == SSM_F32) {
+    // fp32 inputs carry decays as Abar - 1 (two more FMA-pipe operations per state):
+    // one lane per channel amortises the per-step work best; chunks fill the GPU
+    G = cand.front();
   } else {
     // the fewest lanes that reach lane_threads; if even the most cannot, the sequence
     // must be chunked anyway, and one lane per channel (least per-state work) is best
