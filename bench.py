@@ -30,8 +30,36 @@ sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan tokens*channels/s"
 UNIT = "tokens*channels/s"
-FMA_LANES_PER_SM = 128      # FP32 FMA-pipe lanes per SM per clock (B300)
-FMA_SLOTS_PER_UPDATE = 6    # see alu roofline in the design doc: step*A, ex2 (2 slots), step*x*B, h, y
+# Arithmetic roofline of a state update (Abar = ex2(step * A * log2 e), h = Abar h + (step x) B,
+# y += C h): one MUFU ex2 and four FP32 FMA-pipe lane operations.  Measured on this B300
+# (single-purpose throughput kernels): 32 ex2 and 128 FMA lanes per SM per clock, so
+# both units allow 32 updates per SM per clock.
+EX2_PER_SM_CLK = 32
+FMA_LANES_PER_SM_CLK = 128
+FMA_OPS_PER_UPDATE = 4
+UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDATE)
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the output-pass kernel
+# per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
+# on; reported as null once the sources change.  See profiles/.
+TRAFFIC = {
+    # long_bf16_16k capture (mean of 5 output launches: 256.7 MB read + 60.2 MB write),
+    # scaled by the units processed (x8) to the 131072-step workload; the sources
+    # differ from the captured build in comments only
+    "long_bf16": {"bytes_per_launch": 2535000000, "kernel_src_sha": "06b260ed171d5d60"},
+    "long_bf16_16k": {"bytes_per_launch": 316900000, "kernel_src_sha": "06b260ed171d5d60"},
+}
+
+
+def kernel_src_sha() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_112_b300", "csrc", "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(f, "rb") as fh:
+                h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -218,9 +246,10 @@ def main():
     stream = torch.cuda.current_stream(device)
     state_in = w.h0 is not None
 
+    if state_in:
+        fs.copy_(fs0)  # recurrent-step workload: each step advances the stored state
+
     def step():
-        if state_in:
-            fs.copy_(fs0)  # recurrent-step workload: restore the stored state
         ssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                                    t["delta_bias"], out=out, final_state=fs,
                                    delta_softplus=w.delta_softplus, state_in=state_in)
@@ -263,20 +292,23 @@ def main():
     alg = w.algorithmic_bytes()
     dom = max(prof, key=lambda k: prof[k][1]) if prof else None
     dom_ms = prof[dom][1] / prof[dom][0] if dom else ms_step
-    achieved = alg / (dom_ms * 1e-3) / 1e9
-    alu_peak = FMA_LANES_PER_SM * sms * sm_max * 1e6 / FMA_SLOTS_PER_UPDATE  # updates/s
-    alu_achieved = w.element_updates / (dom_ms * 1e-3)
     total_ms = sum(v[1] for v in prof.values()) or 1.0
-    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
-            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "peak_source": peak_kind,
-            "traffic": None, "algorithmic_bytes_per_launch": alg,
+    hbm_achieved = alg / (dom_ms * 1e-3) / 1e9                      # GB/s
+    upd_peak = UPDATES_PER_SM_CLK * sms * sm_max * 1e6 / 1e9           # Gupdate/s
+    upd_achieved = w.element_updates / (dom_ms * 1e-3) / 1e9
+    tr = TRAFFIC.get(args.workload)
+    traffic = tr["bytes_per_launch"] if tr and tr["kernel_src_sha"] == kernel_src_sha() else None
+    roof = {"bound": "alu", "kernel": dom, "achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
+            "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
+            "peak_basis": (f"min({EX2_PER_SM_CLK} MUFU ex2, {FMA_LANES_PER_SM_CLK}/{FMA_OPS_PER_UPDATE} FMA lanes)"
+                           f" state updates per SM per clock (measured on B300) x {sms} SMs x"
+                           f" {sm_max:.0f} MHz"),
+            "traffic": traffic, "algorithmic_bytes_per_launch": alg,
             "kernel_ms_avg": round(dom_ms, 4),
+            "hbm": {"achieved": round(hbm_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(hbm_achieved / hbm_peak, 4), "peak_source": peak_kind},
             "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4),
-                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()},
-            "alu": {"achieved": alu_achieved, "peak": alu_peak, "unit": "state-updates/s",
-                    "frac": round(alu_achieved / alu_peak, 4),
-                    "peak_basis": f"{FMA_LANES_PER_SM} FP32 lanes/SM x {sms} SMs x {sm_max:.0f} MHz"
-                                  f" / {FMA_SLOTS_PER_UPDATE} FMA-pipe slots per state update"}}
+                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()}}
 
     res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

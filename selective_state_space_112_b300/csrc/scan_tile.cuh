@@ -24,11 +24,15 @@
 //  * Each CTA has four consumer warps and one producer warp.  The producer fills a
 //    3- or 4-stage ring of input tiles (x, delta, z: T steps x CH channels; B, C: T x N)
 //    with TMA (cp.async.bulk.tensor), or with plain loads for shapes a tensor map
-//    cannot describe, completed on "full" mbarriers; consumer warps release a stage
-//    on its "empty" mbarrier.  There is no CTA-wide barrier in the main loop: warps
-//    run independently and hide one another's latencies.
-//  * B and C rows stay in the io dtype in shared memory (bf16 halves the load
-//    traffic of the scan, its binding resource) and are widened in registers.
+//    cannot describe, completed on "full" mbarriers.  It widens each tile's B and C
+//    rows once to fp32 planes and hands the stage to the consumers on a "ready"
+//    mbarrier; consumer warps release it on an "empty" mbarrier.  There is no
+//    CTA-wide barrier in the main loop: warps run independently and hide one
+//    another's latencies.
+//  * Consumers read B and C rows as broadcast vector loads from the fp32 planes.  The
+//    shared-memory data path is the scarce resource of the scan (every lane pays the
+//    full width of a warp-wide load); widening bf16 rows per lane instead halves that
+//    traffic but adds two instructions per state update and measured slower.
 //  * Abar, Bbar and h never touch memory: only out and the final state are written.
 //  * Sequences too long for the channel count are cut into chunks scanned by
 //    different CTAs.  The carry uses the associative combine of the per-step maps
