@@ -11,6 +11,7 @@
  *   step_t  = softplus(delta[b,t,d] + delta_bias[d])   (or without softplus)
  *   Abar    = exp(step_t * A[d,n])                      zero-order hold, diagonal A
  *   Bbar x  = step_t * B[.,t,n] * x[b,t,d]              the fused scan's input term
+ *             (bbar_mode 1: (Abar - 1) / A[d,n] * B[.,t,n] * x[b,t,d], exact ZOH)
  *   h_t[n]  = Abar * h_{t-1}[n] + Bbar x                h_{-1} = 0 or a given state
  *   y_t     = sum_n C[.,t,n] h_t[n] + D[d] x[b,t,d]
  *   out     = y_t * silu(z[b,t,d])                      when a gate z is given
@@ -75,8 +76,9 @@ typedef struct {
   int32_t bc_layout;      /* ssm_bc_layout */
   int32_t delta_softplus; /* 1: step = softplus(delta + bias); 0: step = delta + bias */
   int32_t state_in;       /* 1: final_state holds h_{-1} on entry (resume / recurrent step) */
-  int32_t bbar_mode;      /* 0: Bbar = step * B (the only mode built; 1 = exact ZOH is
-                             rejected with SSM_ERR_UNSUPPORTED) */
+  int32_t bbar_mode;      /* 0: Bbar = step * B (the fused scan's input term);
+                             1: exact zero-order hold, Bbar = (exp(step A) - 1) / A * B
+                             (the limit step * B where A = 0) */
   int32_t reserved;       /* must be 0 */
 } ssm_dims;
 

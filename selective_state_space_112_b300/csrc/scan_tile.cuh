@@ -89,6 +89,7 @@ struct ScanParams {
   int delta_softplus;
   int pow_path;
   int use_tma;
+  int bbar_mode;        // 0: Bbar = step B; 1: exact ZOH, Bbar = (exp(step A) - 1) / A B
 };
 
 struct TmaMaps {
@@ -299,6 +300,8 @@ struct LaneConsts {
   float2 A2[S / 2];    // A * log2(e), state pairs
   float Ar[S];         // A (expm1 forms)
   float Bc[S], Cc[S];  // constant-coefficient B and C
+  float2 invA[S / 2];  // exact ZOH: 1 / A (0 where A = 0)
+  float2 zA[S / 2];    // exact ZOH: 1 where A = 0, else 0
 };
 
 // Both halves of a word of two bf16 values, widened exactly to fp32.
@@ -382,13 +385,16 @@ __device__ __forceinline__ void decays(float p1, int g, const LaneConsts<S>& k, 
 }
 
 // One step of one lane: update its S states; return its share of C . h (0 when !OUT).
-template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM>
-__device__ __forceinline__ float lane_step(float p1, float u, const float* __restrict__ brow,
+// u is step * x, or x with the exact-ZOH input term (ZOH), whose factor
+// (Abar - 1) / A (the limit step where A = 0) needs the step size dt.
+template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM, bool ZOH>
+__device__ __forceinline__ float lane_step(float p1, float u, float dt, const float* __restrict__ brow,
                                            const float* __restrict__ crow, int g,
                                            float2 (&h)[S / 2], const LaneConsts<S>& k) {
   float2 a[S / 2];
   decays<S, G, POW, MFORM>(p1, g, k, a);
   const float2 u2 = f2(u, u);
+  const float2 dt2 = f2(dt, dt);
   float2 bv[S / 2], cv[S / 2];
   if (LTI) {
 #pragma unroll
@@ -404,7 +410,12 @@ __device__ __forceinline__ float lane_step(float p1, float u, const float* __res
   float2 ya0 = f2(0.f, 0.f), ya1 = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < S / 2; ++i) {
-    const float2 ub = __fmul2_rn(u2, bv[i]);
+    float2 ub = __fmul2_rn(u2, bv[i]);
+    if (ZOH) {
+      // (Abar - 1) / A, exactly step where A = 0
+      const float2 m = MFORM ? a[i] : __fadd2_rn(a[i], f2(-1.f, -1.f));
+      ub = __fmul2_rn(__ffma2_rn(m, k.invA[i], __fmul2_rn(dt2, k.zA[i])), ub);
+    }
     h[i] = MFORM ? __fadd2_rn(h[i], __ffma2_rn(a[i], h[i], ub)) : __ffma2_rn(a[i], h[i], ub);
     if (OUT) {
       if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
@@ -613,6 +624,14 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       if (j & 1) k.A2[j / 2].y = a * kLog2e;
       else k.A2[j / 2].x = a * kLog2e;
       k.Ar[j] = a;
+      const float ia = (a != 0.f) ? 1.f / a : 0.f, za = (a == 0.f) ? 1.f : 0.f;
+      if (j & 1) {
+        k.invA[j / 2].y = ia;
+        k.zA[j / 2].y = za;
+      } else {
+        k.invA[j / 2].x = ia;
+        k.zA[j / 2].x = za;
+      }
       if (n < N && a != (float)(n + 1) * a0) structured = false;
       if (LTI) {
         k.Bc[j] = (n < N) ? static_cast<const float*>(p.B)[dd * N + n] : 0.f;
@@ -677,8 +696,9 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   //   C  reduce-scatter of the shares, D x, gate, store
   constexpr int R = (G == 1) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
-  auto run = [&](auto pow_tag) -> bool {
+  auto run = [&](auto pow_tag, auto zoh_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value && !LTI;
+    constexpr bool ZOH = decltype(zoh_tag)::value;
     int64_t orow = ((int64_t)b * L + t0) * Dm + d;  // out index of step 0 of the tile, this channel
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % ST;
@@ -689,7 +709,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       const float* brow0 = reinterpret_cast<const float*>(st + Gm::OFF_F) + g * S;
 #pragma unroll
       for (int r0 = 0; r0 < T / G; r0 += R) {
-        float xv[R], p1v[R], uv[R];
+        float xv[R], p1v[R], uv[R], dtv[R];
 #pragma unroll
         for (int q = 0; q < R; ++q) {  // phase A
           const int tm = (r0 + q) * G + g;
@@ -698,7 +718,8 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           const float v = IO::lds(st + XB + xo) + biasv;
           float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
           if (tm >= nvalid) dt = 0.f;  // past the end: identity step
-          uv[q] = dt * xv[q];
+          uv[q] = ZOH ? xv[q] : dt * xv[q];
+          dtv[q] = dt;
           p1v[q] = dt;
           if (POW) p1v[q] = MFORM ? expm1f(dt * eA0) : ex2(dt * eA0 * kLog2e);
           if (PASS == 0) kahan_add(S_sum, S_comp, dt);
@@ -710,9 +731,11 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           for (int j = 0; j < G; ++j) {
             const float pj = (G == 1) ? p1v[q] : __shfl_sync(0xffffffffu, p1v[q], gbase + j);
             const float uj = (G == 1) ? uv[q] : __shfl_sync(0xffffffffu, uv[q], gbase + j);
+            // the exact-ZOH factor needs the step size; it is p1 unless p1 is a power base
+            const float dj = !(ZOH && POW) ? pj : (G == 1) ? dtv[q] : __shfl_sync(0xffffffffu, dtv[q], gbase + j);
             const int t = (r0 + q) * G + j;
-            yv[q][j] = lane_step<S, G, POW, LTI, OUT, MFORM>(pj, uj, brow0 + t * NS,
-                                                             brow0 + Gm::FB / 4 + t * NS, g, h, k);
+            yv[q][j] = lane_step<S, G, POW, LTI, OUT, MFORM, ZOH>(pj, uj, dj, brow0 + t * NS,
+                                                                  brow0 + Gm::FB / 4 + t * NS, g, h, k);
           }
         }
         if (OUT) {
@@ -732,7 +755,11 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     }
     return true;
   };
-  const bool done = use_pow ? run(std::true_type{}) : run(std::false_type{});
+  bool done;
+  if (p.bbar_mode)
+    done = use_pow ? run(std::true_type{}, std::true_type{}) : run(std::false_type{}, std::true_type{});
+  else
+    done = use_pow ? run(std::true_type{}, std::false_type{}) : run(std::false_type{}, std::false_type{});
   if (!done) {
     if (lane == 0) atomicExch(p.status, kStatusTimeout);
     return;

@@ -307,7 +307,6 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
       (d.bbar_mode != 0 && d.bbar_mode != 1) || d.reserved != 0)
     return SSM_ERR_DIMS;
   if (d.state_in && !final_state) return SSM_ERR_DIMS;
-  if (d.bbar_mode == 1) return SSM_ERR_UNSUPPORTED;
   if (d.seqlen > 0 && (!x || !delta || !A || !B || !C || !out)) return SSM_ERR_NULL;
   const void* ptrs[] = {x, delta, A, B, C, D, z, delta_bias, out, final_state};
   for (const void* q : ptrs)
@@ -351,6 +350,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     p.batch = d.batch; p.seqlen = 1; p.dim = d.dim; p.dstate = (int)d.dstate;
     p.nchunks = 1; p.chunk_len = 1;
     p.delta_softplus = d.delta_softplus;
+    p.bbar_mode = d.bbar_mode;
     ssm::TmaMaps maps;
     std::memset(&maps, 0, sizeof maps);
     const int64_t threads = d.batch * d.dim * G;
@@ -372,6 +372,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   p.delta_softplus = d.delta_softplus;
   p.pow_path = (int)g_opt_pow_path.load();
   p.use_tma = pl.tma ? 1 : 0;
+  p.bbar_mode = d.bbar_mode;
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
   p.status = status;

@@ -1,7 +1,8 @@
 // Recurrent step (sequence length 1) of the selective scan: h <- Abar h + Bbar x from
-// a stored state, y = C . h + D x, gated ("State-space models", section "Recurrence
-// and convolution": the recurrent view generates one token per step with constant
-// work; the state (batch, dim, N) is read and written once).
+// a stored state (Bbar = step B, or the exact ZOH (Abar - 1) / A B), y = C . h + D x,
+// gated ("State-space models", section "Recurrence and convolution": the recurrent
+// view generates one token per step with constant work; the state (batch, dim, N) is
+// read and written once).
 //
 // Design: the work is one pass over the state, so the kernel is laid out for the
 // state's bandwidth: one thread per (batch row, channel, 4 consecutive states), the
@@ -30,7 +31,6 @@ __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMa
   const float xv = IO::load(p.x, cc);  // x[b, 0, d]: (batch, 1, dim) is row-major (batch, dim)
   const float v = IO::load(p.delta, cc) + (p.bias ? p.bias[d] : 0.f);
   const float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
-  const float u = dt * xv;
 
   const int n0 = 4 * g;
   float hv[4], a[4], bv[4], cv[4];
@@ -64,12 +64,12 @@ __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMa
   float y = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float bx = u * bv[j];
-    if (MFORM) {
-      hv[j] = hv[j] + fmaf(expm1f(dt * a[j]), hv[j], bx);
-    } else {
-      hv[j] = fmaf(ex2(dt * a[j] * kLog2e), hv[j], bx);
-    }
+    // decay: Abar - 1 by accurate expm1 (fp32 and constant-coefficient inputs), else Abar
+    const float e = MFORM ? expm1f(dt * a[j]) : ex2(dt * a[j] * kLog2e);
+    // input factor: step (fused scan) or exact ZOH (Abar - 1) / A, step where A = 0
+    const float q = p.bbar_mode ? (a[j] != 0.f ? (MFORM ? e : e - 1.f) / a[j] : dt) : dt;
+    const float bx = q * xv * bv[j];
+    hv[j] = MFORM ? hv[j] + fmaf(e, hv[j], bx) : fmaf(e, hv[j], bx);
     y = fmaf(cv[j], hv[j], y);
   }
 #pragma unroll

@@ -28,7 +28,7 @@ def device_inputs(w, device="cuda"):
     return dev
 
 
-def run_gpu(w, dev=None, out=None):
+def run_gpu(w, dev=None, out=None, bbar_mode=0):
     """Run the CUDA path; return (out, final_state) as float64 numpy arrays."""
     import torch
     import selective_state_space_112_b300 as ssm
@@ -37,18 +37,18 @@ def run_gpu(w, dev=None, out=None):
     o, f = ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
                                       dev["D"], dev["z"], dev["delta_bias"], out=out,
                                       final_state=fs, delta_softplus=w.delta_softplus,
-                                      state_in=w.h0 is not None)
+                                      state_in=w.h0 is not None, bbar_mode=bbar_mode)
     assert ssm.ssm_check_status() == 0
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), f.cpu().numpy().astype(np.float64)
 
 
-def run_oracle(w, threads=0):
+def run_oracle(w, threads=0, bbar_mode=0):
     return oracle.selective_scan(w.x, w.delta, w.A, w.B, w.C, D=w.D, z=w.z,
                                  delta_bias=w.delta_bias, h0=w.h0,
                                  delta_softplus=w.delta_softplus,
                                  per_channel_bc=w.per_channel_bc, io_dtype=w.io,
-                                 threads=threads)
+                                 threads=threads, bbar_mode=bbar_mode)
 
 
 def assert_close(got, ref, io, what="", floor=None):

@@ -271,6 +271,41 @@ def test_device_errors_are_reported():
     assert e.value.code == -6
     with pytest.raises(ssm.SSMError) as e:
         ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
-                                   bbar_mode=1)
-    assert e.value.code == -4
+                                   bbar_mode=2)
+    assert e.value.code == -2
     assert ssm.ssm_check_status() == 0
+
+
+ZOH_CASES = [
+    # (name, make_workload kwargs, lanes, chunks)
+    ("tv_G1_chunks", dict(batch=2, seqlen=700, dim=64, dstate=16), 1, 3),
+    ("tv_G2", dict(batch=2, seqlen=300, dim=96, dstate=16), 2, 0),
+    ("tv_G4_ragged", dict(batch=1, seqlen=77, dim=40, dstate=16, state_in=True), 4, 0),
+    ("s4d_pow_G2", dict(batch=2, seqlen=400, dim=64, dstate=16, a_init="s4d_real"), 2, 2),
+    ("s4d_pow_G1", dict(batch=2, seqlen=400, dim=64, dstate=16, a_init="s4d_real"), 1, 2),
+    ("lti", dict(batch=2, seqlen=300, dim=40, dstate=16, lti=True, with_bias=False), 0, 2),
+    ("N13", dict(batch=2, seqlen=90, dim=24, dstate=13), 0, 2),
+    ("step", dict(batch=8, seqlen=1, dim=136, dstate=16, state_in=True), 0, 0),
+]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("name,kw,lanes,chunks", ZOH_CASES, ids=[c[0] for c in ZOH_CASES])
+def test_exact_zoh(name, kw, lanes, chunks, io):
+    """bbar_mode = 1: Bbar = (exp(step A) - 1) / A * B, the exact zero-order hold
+    ("State-space models", Discretization), against the oracle's exact-ZOH path, on
+    every lane split, the powers path, chunks, the LTI layout, ragged shapes and the
+    recurrent step; one channel of A holds exact zeros (the limit Bbar = step B)."""
+    import selective_state_space_112_b300 as ssm
+    w = make_workload(name, io=io, seed=zlib.crc32(("zoh" + name + io).encode()) % 1000, **kw)
+    if kw.get("a_init") != "s4d_real":
+        w.A[0, ::3] = 0.0
+    ssm.ssm_set_option("lanes", lanes)
+    ssm.ssm_set_option("chunks", chunks)
+    g_out, g_fs = run_gpu(w, bbar_mode=1)
+    r_out, r_fs = run_oracle(w, bbar_mode=1)
+    assert_close(g_out, r_out, w.io, f"{name}/{io} zoh out")
+    assert_close(g_fs, r_fs, w.io, f"{name}/{io} zoh final_state")
+    # the two input terms differ: the check above is not the bbar_mode 0 result
+    r0, _ = run_oracle(w, bbar_mode=0)
+    assert floored_rel_err(r0, r_out) > 2 * TOL[w.io]
