@@ -61,7 +61,7 @@ namespace ssm {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kSpinLimit = 1ll << 30;  // bounded mbarrier polls (backstop)
-constexpr uint64_t kWaitNs = 2000000000ull;  // give up a copy wait after 2 s
+constexpr uint64_t kWaitNs = 2000000000ull;  // default bound of a copy wait: 2 s
 constexpr int kChunkAlign = 32;              // chunk lengths are multiples of this (>= every T)
 
 enum : int { kStatusOk = 0, kStatusTimeout = 1 };
@@ -90,6 +90,9 @@ struct ScanParams {
   int pow_path;
   int use_tma;
   int bbar_mode;        // 0: Bbar = step B; 1: exact ZOH, Bbar = (exp(step A) - 1) / A B
+  uint64_t wait_ns;     // bound of every copy wait (kWaitNs unless a test shortens it)
+  int stall_tile;       // failure injection for tests: the producer stops before this
+                        // tile and never hands it over (-1: off)
 };
 
 struct TmaMaps {
@@ -220,13 +223,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: false if the phase did not complete within kWaitNs (or kSpinLimit polls).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait: false if the phase did not complete within limit_ns (or kSpinLimit polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = globaltimer_ns();
   for (long long i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - start > kWaitNs) return false;
+    if (globaltimer_ns() - start > limit_ns) return false;
   }
   return false;
 }
@@ -500,7 +503,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       const int sj = j % ST;
       if (j >= ST) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[sj], ((j / ST) - 1) & 1);
+        if (lane == 0) ok = mbar_wait(&empty[sj], ((j / ST) - 1) & 1, p.wait_ns);
         if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       }
       unsigned char* st = stage(j);
@@ -583,26 +586,27 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       }
     };
     bool ok = true;
+    int waited = 0;  // tiles whose arrival this warp has already waited for
     for (int j = 0; j < ST - 1 && j < ntiles && ok; ++j) ok = issue(j);
     for (int i = 0; i < ntiles && ok; ++i) {
+      if (i == p.stall_tile) break;  // injected stall: tile i is never handed over
       bool landed = true;
-      if (lane == 0) landed = mbar_wait(&full[i % ST], (i / ST) & 1);
+      if (lane == 0) landed = mbar_wait(&full[i % ST], (i / ST) & 1, p.wait_ns);
       if (!__shfl_sync(0xffffffffu, landed, 0)) {
         ok = false;
         break;
       }
+      waited = i + 1;
       widen(i);
       __threadfence_block();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ready[i % ST]);
       if (i + ST - 1 < ntiles) ok = issue(i + ST - 1);
     }
-    if (!ok && lane == 0) {
-      atomicExch(p.status, kStatusTimeout);
+    if (!ok && lane == 0) atomicExch(p.status, kStatusTimeout);
+    if (lane == 0 && tma)
       // let the copies still in flight land (each wait bounded) before leaving
-      if (tma)
-        for (int j = max(0, issued - ST); j < issued; ++j) mbar_wait(&full[j % ST], (j / ST) & 1);
-    }
+      for (int j = waited; j < issued; ++j) mbar_wait(&full[j % ST], (j / ST) & 1, p.wait_ns);
     return;
   }
 
@@ -702,7 +706,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     int64_t orow = ((int64_t)b * L + t0) * Dm + d;  // out index of step 0 of the tile, this channel
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % ST;
-      if (!mbar_wait(&ready[s], (i / ST) & 1)) return false;
+      if (!mbar_wait(&ready[s], (i / ST) & 1, p.wait_ns)) return false;
       const unsigned char* st = stage(i);
       const int64_t ts = t0 + (int64_t)i * T;
       const int nvalid = (int)min((int64_t)T, t1 - ts);

@@ -31,6 +31,8 @@ std::atomic<int64_t> g_opt_lane_threads{32768};
 std::atomic<int64_t> g_opt_ctas_per_sm{3};
 std::atomic<int64_t> g_opt_pow_path{1};
 std::atomic<int64_t> g_opt_tma{1};
+std::atomic<int64_t> g_opt_wait_ns{0};       // 0: the kernels' default bound
+std::atomic<int64_t> g_opt_inject_stall{0};  // tests: 1 + tile index the producer withholds
 std::atomic<uint64_t> g_launches{0};
 
 __device__ int g_status;  // raised by a kernel: kStatusTimeout, or any other nonzero value
@@ -373,6 +375,8 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   p.pow_path = (int)g_opt_pow_path.load();
   p.use_tma = pl.tma ? 1 : 0;
   p.bbar_mode = d.bbar_mode;
+  p.wait_ns = g_opt_wait_ns.load() > 0 ? (uint64_t)g_opt_wait_ns.load() : ssm::kWaitNs;
+  p.stall_tile = (int)g_opt_inject_stall.load() - 1;
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
   p.status = status;
@@ -469,6 +473,8 @@ int ssm_set_option(const char* name, int64_t value) {
   else if (!std::strcmp(name, "ctas_per_sm")) g_opt_ctas_per_sm = value;
   else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
   else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;
+  else if (!std::strcmp(name, "wait_ns")) g_opt_wait_ns = value;
+  else if (!std::strcmp(name, "inject_stall")) g_opt_inject_stall = std::min<int64_t>(value, INT32_MAX);
   else return SSM_ERR_DIMS;
   return SSM_OK;
 }
