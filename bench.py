@@ -203,6 +203,19 @@ def cpu_baseline(w, budget_s: float = 15.0):
                       f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (the job's time is the slowest rank's)."""
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, steps: int, ms_max: float, world: int) -> float:
+    """Whole-job units per second: every rank ran its own replica of the workload."""
+    return world * units_per_rank * steps / (ms_max * 1e-3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -278,13 +291,11 @@ def main():
     assert ssm.ssm_check_status() == 0
     ms = ev0.elapsed_time(ev1)
     if world > 1:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, device)
         dist.barrier()
     ms_step = ms / args.steps
     units = w.tokens_channels
-    value = world * units * args.steps / (ms * 1e-3)
+    value = job_throughput(units, args.steps, ms, world)
 
     # ---- roofline of the dominant kernel (CUDA events recorded around each launch)
     hbm_peak, sm_max, peak_kind = load_peaks()
@@ -356,10 +367,8 @@ def main():
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
         if world > 1:
-            tt = torch.tensor([ems], device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
-        res["e2e"] = {"value": world * units * args.e2e_steps / (ems * 1e-3), "unit": UNIT,
+            ems = max_over_ranks(ems, dist, device)
+        res["e2e"] = {"value": job_throughput(units, args.e2e_steps, ems, world), "unit": UNIT,
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": ems / args.e2e_steps}
 
