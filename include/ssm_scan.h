@@ -175,12 +175,11 @@ uint64_t ssm_kernel_launches(void);
  *                   0: always one exponential per state
  *   "tma"           1 (default): use the TMA-pipelined kernel where tensor maps can
  *                   describe the tensors; 0: always the generic kernel
- *   "wait_ns"       bound of every wait of a kernel for its own copies, in ns
- *                   (0 = the default 2 s); a wait that runs out raises SSM_ERR_TIMEOUT
  *   "inject_stall"  failure injection for tests (0 = off): with value k, the copy
  *                   producer of every CTA stops before its tile k - 1, so the waits
- *                   for that tile run out; the kernels return and ssm_check_status
- *                   reports SSM_ERR_TIMEOUT.  Leave it 0 otherwise.
+ *                   for that tile run out (every wait of a kernel is bounded by 2 s);
+ *                   the kernels return and ssm_check_status reports SSM_ERR_TIMEOUT.
+ *                   Leave it 0 otherwise.
  * Returns SSM_ERR_DIMS for an unknown name or a negative value.
  */
 int ssm_set_option(const char* name, int64_t value);

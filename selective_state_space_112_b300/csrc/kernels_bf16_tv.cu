@@ -1,6 +1,6 @@
-// Instantiations of the tiled selective-scan kernel: bf16 inputs, time-varying B and C.
+// Instantiations of the tiled selective-scan kernel: bf16 inputs, time-varying B and C, the fused scan's input term step * B.
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_bf16_tv(int S, int G, int pass) { return lookup_impl<BF16, false>(S, G, pass); }
+KernelInfo lookup_bf16_tv(int S, int G, int pass) { return lookup_impl<BF16, false, false>(S, G, pass); }
 }  // namespace ssm

@@ -1,6 +1,6 @@
-// Instantiations of the tiled selective-scan kernel: f32 inputs, time-varying B and C.
+// Instantiations of the tiled selective-scan kernel: f32 inputs, time-varying B and C, the fused scan's input term step * B.
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_f32_tv(int S, int G, int pass) { return lookup_impl<F32, false>(S, G, pass); }
+KernelInfo lookup_f32_tv(int S, int G, int pass) { return lookup_impl<F32, false, false>(S, G, pass); }
 }  // namespace ssm

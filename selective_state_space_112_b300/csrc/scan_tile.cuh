@@ -61,7 +61,7 @@ namespace ssm {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kSpinLimit = 1ll << 30;  // bounded mbarrier polls (backstop)
-constexpr uint64_t kWaitNs = 2000000000ull;  // default bound of a copy wait: 2 s
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound of a copy wait: 2 s
 constexpr int kChunkAlign = 32;              // chunk lengths are multiples of this (>= every T)
 
 enum : int { kStatusOk = 0, kStatusTimeout = 1 };
@@ -90,7 +90,6 @@ struct ScanParams {
   int pow_path;
   int use_tma;
   int bbar_mode;        // 0: Bbar = step B; 1: exact ZOH, Bbar = (exp(step A) - 1) / A B
-  uint64_t wait_ns;     // bound of every copy wait (kWaitNs unless a test shortens it)
   int stall_tile;       // failure injection for tests: the producer stops before this
                         // tile and never hands it over (-1: off)
 };
@@ -223,13 +222,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: false if the phase did not complete within limit_ns (or kSpinLimit polls).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+// Bounded wait: false if the phase did not complete within kWaitNs (or kSpinLimit polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = globaltimer_ns();
   for (long long i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - start > limit_ns) return false;
+    if (globaltimer_ns() - start > kWaitNs) return false;
   }
   return false;
 }
@@ -388,16 +387,15 @@ __device__ __forceinline__ void decays(float p1, int g, const LaneConsts<S>& k, 
 }
 
 // One step of one lane: update its S states; return its share of C . h (0 when !OUT).
-// u is step * x, or x with the exact-ZOH input term (ZOH), whose factor
-// (Abar - 1) / A (the limit step where A = 0) needs the step size dt.
-template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM, bool ZOH>
-__device__ __forceinline__ float lane_step(float p1, float u, float dt, const float* __restrict__ brow,
+// One step of one lane: update its S states; return its share of C . h (0 when !OUT).
+// u = step * x.
+template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM>
+__device__ __forceinline__ float lane_step(float p1, float u, const float* __restrict__ brow,
                                            const float* __restrict__ crow, int g,
                                            float2 (&h)[S / 2], const LaneConsts<S>& k) {
   float2 a[S / 2];
   decays<S, G, POW, MFORM>(p1, g, k, a);
   const float2 u2 = f2(u, u);
-  const float2 dt2 = f2(dt, dt);
   float2 bv[S / 2], cv[S / 2];
   if (LTI) {
 #pragma unroll
@@ -413,12 +411,42 @@ __device__ __forceinline__ float lane_step(float p1, float u, float dt, const fl
   float2 ya0 = f2(0.f, 0.f), ya1 = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < S / 2; ++i) {
-    float2 ub = __fmul2_rn(u2, bv[i]);
-    if (ZOH) {
-      // (Abar - 1) / A, exactly step where A = 0
-      const float2 m = MFORM ? a[i] : __fadd2_rn(a[i], f2(-1.f, -1.f));
-      ub = __fmul2_rn(__ffma2_rn(m, k.invA[i], __fmul2_rn(dt2, k.zA[i])), ub);
+    const float2 ub = __fmul2_rn(u2, bv[i]);
+    h[i] = MFORM ? __fadd2_rn(h[i], __ffma2_rn(a[i], h[i], ub)) : __ffma2_rn(a[i], h[i], ub);
+    if (OUT) {
+      if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
+      else ya0 = __ffma2_rn(cv[i], h[i], ya0);
     }
+  }
+  return OUT ? (ya0.x + ya0.y) + (ya1.x + ya1.y) : 0.f;
+}
+
+// The same step with the exact zero-order-hold input term: u = x, and Bbar = q B with
+// q = (Abar - 1) / A, exactly the step size dt where A = 0.
+template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM>
+__device__ __forceinline__ float lane_step_zoh(float p1, float u, float dt, const float* __restrict__ brow,
+                                               const float* __restrict__ crow, int g,
+                                               float2 (&h)[S / 2], const LaneConsts<S>& k) {
+  float2 a[S / 2];
+  decays<S, G, POW, MFORM>(p1, g, k, a);
+  const float2 u2 = f2(u, u), dt2 = f2(dt, dt);
+  float2 bv[S / 2], cv[S / 2];
+  if (LTI) {
+#pragma unroll
+    for (int i = 0; i < S / 2; ++i) {
+      bv[i] = f2(k.Bc[2 * i], k.Bc[2 * i + 1]);
+      cv[i] = f2(k.Cc[2 * i], k.Cc[2 * i + 1]);
+    }
+  } else {
+    load_row<F32, S>(reinterpret_cast<const unsigned char*>(brow), bv);
+    if (OUT) load_row<F32, S>(reinterpret_cast<const unsigned char*>(crow), cv);
+  }
+  float2 ya0 = f2(0.f, 0.f), ya1 = f2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < S / 2; ++i) {
+    const float2 m = MFORM ? a[i] : __fadd2_rn(a[i], f2(-1.f, -1.f));
+    const float2 q = __ffma2_rn(m, k.invA[i], __fmul2_rn(dt2, k.zA[i]));
+    const float2 ub = __fmul2_rn(q, __fmul2_rn(u2, bv[i]));
     h[i] = MFORM ? __fadd2_rn(h[i], __ffma2_rn(a[i], h[i], ub)) : __ffma2_rn(a[i], h[i], ub);
     if (OUT) {
       if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
@@ -452,7 +480,9 @@ __device__ __forceinline__ float reduce_scatter(const float (&v)[G], int g) {
 // PASS 0: chunk aggregate (end state from a zero start, sum of steps) of chunks
 //         0 .. nchunks-2.
 // PASS 1: output pass (carry-in, out, final state).
-template <typename IO, int S, int G, bool LTI, int PASS>
+// ZOH: exact zero-order-hold input term (bbar_mode 1), a separate instantiation so
+// that the common path carries none of its registers.
+template <typename IO, int S, int G, bool LTI, int PASS, bool ZOH>
 __global__ void __launch_bounds__(Geo<IO, S, G>::NT)
 scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   using Gm = Geo<IO, S, G>;
@@ -503,7 +533,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       const int sj = j % ST;
       if (j >= ST) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[sj], ((j / ST) - 1) & 1, p.wait_ns);
+        if (lane == 0) ok = mbar_wait(&empty[sj], ((j / ST) - 1) & 1);
         if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       }
       unsigned char* st = stage(j);
@@ -591,7 +621,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     for (int i = 0; i < ntiles && ok; ++i) {
       if (i == p.stall_tile) break;  // injected stall: tile i is never handed over
       bool landed = true;
-      if (lane == 0) landed = mbar_wait(&full[i % ST], (i / ST) & 1, p.wait_ns);
+      if (lane == 0) landed = mbar_wait(&full[i % ST], (i / ST) & 1);
       if (!__shfl_sync(0xffffffffu, landed, 0)) {
         ok = false;
         break;
@@ -606,7 +636,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     if (!ok && lane == 0) atomicExch(p.status, kStatusTimeout);
     if (lane == 0 && tma)
       // let the copies still in flight land (each wait bounded) before leaving
-      for (int j = waited; j < issued; ++j) mbar_wait(&full[j % ST], (j / ST) & 1, p.wait_ns);
+      for (int j = waited; j < issued; ++j) mbar_wait(&full[j % ST], (j / ST) & 1);
     return;
   }
 
@@ -628,13 +658,15 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       if (j & 1) k.A2[j / 2].y = a * kLog2e;
       else k.A2[j / 2].x = a * kLog2e;
       k.Ar[j] = a;
-      const float ia = (a != 0.f) ? 1.f / a : 0.f, za = (a == 0.f) ? 1.f : 0.f;
-      if (j & 1) {
-        k.invA[j / 2].y = ia;
-        k.zA[j / 2].y = za;
-      } else {
-        k.invA[j / 2].x = ia;
-        k.zA[j / 2].x = za;
+      if (ZOH) {
+        const float ia = (a != 0.f) ? 1.f / a : 0.f, za = (a == 0.f) ? 1.f : 0.f;
+        if (j & 1) {
+          k.invA[j / 2].y = ia;
+          k.zA[j / 2].y = za;
+        } else {
+          k.invA[j / 2].x = ia;
+          k.zA[j / 2].x = za;
+        }
       }
       if (n < N && a != (float)(n + 1) * a0) structured = false;
       if (LTI) {
@@ -700,20 +732,20 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   //   C  reduce-scatter of the shares, D x, gate, store
   constexpr int R = (G == 1) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
-  auto run = [&](auto pow_tag, auto zoh_tag) -> bool {
+  auto run = [&](auto pow_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value && !LTI;
-    constexpr bool ZOH = decltype(zoh_tag)::value;
     int64_t orow = ((int64_t)b * L + t0) * Dm + d;  // out index of step 0 of the tile, this channel
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % ST;
-      if (!mbar_wait(&ready[s], (i / ST) & 1, p.wait_ns)) return false;
+      if (!mbar_wait(&ready[s], (i / ST) & 1)) return false;
       const unsigned char* st = stage(i);
       const int64_t ts = t0 + (int64_t)i * T;
       const int nvalid = (int)min((int64_t)T, t1 - ts);
       const float* brow0 = reinterpret_cast<const float*>(st + Gm::OFF_F) + g * S;
 #pragma unroll
       for (int r0 = 0; r0 < T / G; r0 += R) {
-        float xv[R], p1v[R], uv[R], dtv[R];
+        float xv[R], p1v[R], uv[R];
+        [[maybe_unused]] float dtv[ZOH ? R : 1];
 #pragma unroll
         for (int q = 0; q < R; ++q) {  // phase A
           const int tm = (r0 + q) * G + g;
@@ -722,8 +754,12 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           const float v = IO::lds(st + XB + xo) + biasv;
           float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
           if (tm >= nvalid) dt = 0.f;  // past the end: identity step
-          uv[q] = ZOH ? xv[q] : dt * xv[q];
-          dtv[q] = dt;
+          if constexpr (ZOH) {
+            uv[q] = xv[q];
+            dtv[q] = dt;
+          } else {
+            uv[q] = dt * xv[q];
+          }
           p1v[q] = dt;
           if (POW) p1v[q] = MFORM ? expm1f(dt * eA0) : ex2(dt * eA0 * kLog2e);
           if (PASS == 0) kahan_add(S_sum, S_comp, dt);
@@ -735,11 +771,16 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           for (int j = 0; j < G; ++j) {
             const float pj = (G == 1) ? p1v[q] : __shfl_sync(0xffffffffu, p1v[q], gbase + j);
             const float uj = (G == 1) ? uv[q] : __shfl_sync(0xffffffffu, uv[q], gbase + j);
-            // the exact-ZOH factor needs the step size; it is p1 unless p1 is a power base
-            const float dj = !(ZOH && POW) ? pj : (G == 1) ? dtv[q] : __shfl_sync(0xffffffffu, dtv[q], gbase + j);
             const int t = (r0 + q) * G + j;
-            yv[q][j] = lane_step<S, G, POW, LTI, OUT, MFORM, ZOH>(pj, uj, dj, brow0 + t * NS,
-                                                                  brow0 + Gm::FB / 4 + t * NS, g, h, k);
+            if constexpr (ZOH) {
+              // the exact-ZOH factor needs the step size: p1 unless p1 is a power base
+              const float dj = !POW ? pj : (G == 1) ? dtv[q] : __shfl_sync(0xffffffffu, dtv[q], gbase + j);
+              yv[q][j] = lane_step_zoh<S, G, POW, LTI, OUT, MFORM>(pj, uj, dj, brow0 + t * NS,
+                                                                   brow0 + Gm::FB / 4 + t * NS, g, h, k);
+            } else {
+              yv[q][j] = lane_step<S, G, POW, LTI, OUT, MFORM>(pj, uj, brow0 + t * NS,
+                                                               brow0 + Gm::FB / 4 + t * NS, g, h, k);
+            }
           }
         }
         if (OUT) {
@@ -759,11 +800,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     }
     return true;
   };
-  bool done;
-  if (p.bbar_mode)
-    done = use_pow ? run(std::true_type{}, std::true_type{}) : run(std::false_type{}, std::true_type{});
-  else
-    done = use_pow ? run(std::true_type{}, std::false_type{}) : run(std::false_type{}, std::false_type{});
+  const bool done = use_pow ? run(std::true_type{}) : run(std::false_type{});
   if (!done) {
     if (lane == 0) atomicExch(p.status, kStatusTimeout);
     return;

@@ -31,7 +31,6 @@ std::atomic<int64_t> g_opt_lane_threads{32768};
 std::atomic<int64_t> g_opt_ctas_per_sm{3};
 std::atomic<int64_t> g_opt_pow_path{1};
 std::atomic<int64_t> g_opt_tma{1};
-std::atomic<int64_t> g_opt_wait_ns{0};       // 0: the kernels' default bound
 std::atomic<int64_t> g_opt_inject_stall{0};  // tests: 1 + tile index the producer withholds
 std::atomic<uint64_t> g_launches{0};
 
@@ -85,7 +84,11 @@ struct Plan {
   ssm::KernelInfo out_k, agg_k;
 };
 
-ssm::KernelInfo lookup(int io, bool lti, int S, int G, int pass) {
+ssm::KernelInfo lookup(int io, bool lti, int S, int G, int pass, bool zoh) {
+  if (zoh) {
+    if (io == SSM_F32) return lti ? ssm::lookup_f32_lti_zoh(S, G, pass) : ssm::lookup_f32_tv_zoh(S, G, pass);
+    return lti ? ssm::lookup_bf16_lti_zoh(S, G, pass) : ssm::lookup_bf16_tv_zoh(S, G, pass);
+  }
   if (io == SSM_F32) return lti ? ssm::lookup_f32_lti(S, G, pass) : ssm::lookup_f32_tv(S, G, pass);
   return lti ? ssm::lookup_bf16_lti(S, G, pass) : ssm::lookup_bf16_tv(S, G, pass);
 }
@@ -156,7 +159,7 @@ bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
   std::vector<int> cand;
   for (int G = 1; G <= 4; G *= 2) {
     const int S = ns / G;
-    if (S >= 2 && S <= 16 && lookup(d.io_dtype, lti, S, G, 1).fn) cand.push_back(G);
+    if (S >= 2 && S <= 16 && lookup(d.io_dtype, lti, S, G, 1, false).fn) cand.push_back(G);
   }
   if (cand.empty()) return false;
   const int64_t forced = g_opt_lanes.load();
@@ -181,8 +184,8 @@ bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
   }
   pl->G = G;
   pl->S = ns / G;
-  pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1);
-  pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0);
+  pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1, d.bbar_mode == 1);
+  pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0, d.bbar_mode == 1);
   pl->tma = g_opt_tma.load() && tma_ok(d);
   int64_t k = g_opt_chunks.load();
   if (k <= 0) {
@@ -375,7 +378,6 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   p.pow_path = (int)g_opt_pow_path.load();
   p.use_tma = pl.tma ? 1 : 0;
   p.bbar_mode = d.bbar_mode;
-  p.wait_ns = g_opt_wait_ns.load() > 0 ? (uint64_t)g_opt_wait_ns.load() : ssm::kWaitNs;
   p.stall_tile = (int)g_opt_inject_stall.load() - 1;
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
@@ -473,7 +475,6 @@ int ssm_set_option(const char* name, int64_t value) {
   else if (!std::strcmp(name, "ctas_per_sm")) g_opt_ctas_per_sm = value;
   else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
   else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;
-  else if (!std::strcmp(name, "wait_ns")) g_opt_wait_ns = value;
   else if (!std::strcmp(name, "inject_stall")) g_opt_inject_stall = std::min<int64_t>(value, INT32_MAX);
   else return SSM_ERR_DIMS;
   return SSM_OK;

@@ -113,7 +113,6 @@ def test_options():
     _abi.set_option("min_chunk_len", 512)
     _abi.set_option("lane_threads", 36864)
     _abi.set_option("ctas_per_sm", 3)
-    _abi.set_option("wait_ns", 0)
     _abi.set_option("inject_stall", 0)
     _abi.set_option("pow_path", 1)
     _abi.set_option("tma", 1)

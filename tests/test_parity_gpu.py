@@ -313,14 +313,13 @@ def test_exact_zoh(name, kw, lanes, chunks, io):
 
 def test_copy_wait_timeout_is_reported_and_the_context_stays_usable():
     """Failure detection without a GPU fault: the copy producer is told to withhold one
-    tile, so the consumer warps' bounded waits run out (50 ms here).  The kernels
+    tile, so the consumer warps' bounded waits run out (after 2 s).  The kernels
     return, ssm_check_status reports SSM_ERR_TIMEOUT, and the next call is correct."""
     import torch
     import selective_state_space_112_b300 as ssm
     w = make_workload("stall", batch=1, seqlen=600, dim=128, dstate=16, io="bf16", seed=8)
     dev = device_inputs(w)
     try:
-        ssm.ssm_set_option("wait_ns", 50_000_000)
         ssm.ssm_set_option("inject_stall", 3)
         ssm.ssm_set_option("chunks", 1)
         ssm.ssm_selective_scan_fwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"],
@@ -329,7 +328,6 @@ def test_copy_wait_timeout_is_reported_and_the_context_stays_usable():
         assert ssm.ssm_check_status() == 0   # read once, then cleared
     finally:
         ssm.ssm_set_option("inject_stall", 0)
-        ssm.ssm_set_option("wait_ns", 0)
         ssm.ssm_set_option("chunks", 0)
     torch.cuda.synchronize()
     full_check(w, "after timeout")
