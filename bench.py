@@ -43,11 +43,10 @@ UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDA
 # per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
 # on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (mean of 5 output launches: 256.7 MB read + 60.2 MB write),
-    # scaled by the units processed (x8) to the 131072-step workload; the sources
-    # differ from the captured build in comments only
-    "long_bf16": {"bytes_per_launch": 2535000000, "kernel_src_sha": "06b260ed171d5d60"},
-    "long_bf16_16k": {"bytes_per_launch": 316900000, "kernel_src_sha": "06b260ed171d5d60"},
+    # long_bf16_16k capture (mean of 5 output launches: 256.66 MB read + 60.09 MB write),
+    # scaled by the units processed (x8) to the 131072-step workload
+    "long_bf16": {"bytes_per_launch": 2534000000, "kernel_src_sha": "cf512725049333a9"},
+    "long_bf16_16k": {"bytes_per_launch": 316750000, "kernel_src_sha": "cf512725049333a9"},
 }
 
 
