@@ -96,6 +96,7 @@ struct ScanParams {
 
 struct TmaMaps {
   CUtensorMap x, delta, z, B, C;
+  CUtensorMap out;  // box of the x tile: the output pass stores y tiles with it
 };
 
 // ------------------------------------------------------------------ element access
@@ -386,7 +387,21 @@ __device__ __forceinline__ void decays(float p1, int g, const LaneConsts<S>& k, 
   }
 }
 
-// One step of one lane: update its S states; return its share of C . h (0 when !OUT).
+// This lane's share of C . h: two accumulators (half the dependent chain), each
+// started from a product rather than from zero.
+template <int S>
+__device__ __forceinline__ float readout(const float2 (&cv)[S / 2], const float2 (&h)[S / 2]) {
+  float2 ya0 = __fmul2_rn(cv[0], h[0]);
+  if (S == 2) return ya0.x + ya0.y;
+  float2 ya1 = __fmul2_rn(cv[1], h[1]);
+#pragma unroll
+  for (int i = 2; i < S / 2; ++i) {
+    if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
+    else ya0 = __ffma2_rn(cv[i], h[i], ya0);
+  }
+  return (ya0.x + ya0.y) + (ya1.x + ya1.y);
+}
+
 // One step of one lane: update its S states; return its share of C . h (0 when !OUT).
 // u = step * x.
 template <int S, int G, bool POW, bool LTI, bool OUT, bool MFORM>
@@ -407,18 +422,12 @@ __device__ __forceinline__ float lane_step(float p1, float u, const float* __res
     load_row<F32, S>(reinterpret_cast<const unsigned char*>(brow), bv);
     if (OUT) load_row<F32, S>(reinterpret_cast<const unsigned char*>(crow), cv);
   }
-  // two accumulators: halves the dependent chain of the readout
-  float2 ya0 = f2(0.f, 0.f), ya1 = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < S / 2; ++i) {
     const float2 ub = __fmul2_rn(u2, bv[i]);
     h[i] = MFORM ? __fadd2_rn(h[i], __ffma2_rn(a[i], h[i], ub)) : __ffma2_rn(a[i], h[i], ub);
-    if (OUT) {
-      if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
-      else ya0 = __ffma2_rn(cv[i], h[i], ya0);
-    }
   }
-  return OUT ? (ya0.x + ya0.y) + (ya1.x + ya1.y) : 0.f;
+  return OUT ? readout<S>(cv, h) : 0.f;
 }
 
 // The same step with the exact zero-order-hold input term: u = x, and Bbar = q B with
@@ -441,19 +450,14 @@ __device__ __forceinline__ float lane_step_zoh(float p1, float u, float dt, cons
     load_row<F32, S>(reinterpret_cast<const unsigned char*>(brow), bv);
     if (OUT) load_row<F32, S>(reinterpret_cast<const unsigned char*>(crow), cv);
   }
-  float2 ya0 = f2(0.f, 0.f), ya1 = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < S / 2; ++i) {
     const float2 m = MFORM ? a[i] : __fadd2_rn(a[i], f2(-1.f, -1.f));
     const float2 q = __ffma2_rn(m, k.invA[i], __fmul2_rn(dt2, k.zA[i]));
     const float2 ub = __fmul2_rn(q, __fmul2_rn(u2, bv[i]));
     h[i] = MFORM ? __fadd2_rn(h[i], __ffma2_rn(a[i], h[i], ub)) : __ffma2_rn(a[i], h[i], ub);
-    if (OUT) {
-      if (i & 1) ya1 = __ffma2_rn(cv[i], h[i], ya1);
-      else ya0 = __ffma2_rn(cv[i], h[i], ya0);
-    }
   }
-  return OUT ? (ya0.x + ya0.y) + (ya1.x + ya1.y) : 0.f;
+  return OUT ? readout<S>(cv, h) : 0.f;
 }
 
 // Lane g of a group of G lanes gets sum over the group of v[g]: a butterfly
@@ -525,17 +529,54 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   // Keeps ST - 1 tiles in flight ahead of the consumers: issues the copies of tile
   // i + ST - 1 once the consumers have released its stage, and widens the B / C rows
   // of tile i to fp32 planes (once per CTA, not once per lane) before releasing it.
+  // In the output pass the consumers leave y of each step in place of its x in the
+  // stage; the producer copies the released tile to out before refilling the stage.
   if (warp == NW) {
     const uint32_t tile_bytes =
         (uint32_t)((2 + (gate ? 1 : 0)) * T * CH * ESZ + (LTI ? 0 : (OUT ? 2 : 1) * T * N * ESZ));
+    const bool sp = p.delta_softplus != 0;
     int issued = 0;
+    int released = 0;  // tiles whose stage the consumers have handed back
+    // all lanes call: waits until the consumers release tile j; in the output pass
+    // copies its y to out (a bulk tensor copy clipped at the sequence end and the last
+    // channel, or plain stores); false if the wait ran out
+    auto release = [&](int j) {
+      const int sj = j % ST;
+      const uint32_t par = (j / ST) & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[sj], par);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      released = j + 1;
+      if (!OUT) return true;
+      const unsigned char* st = stage(j);
+      const int64_t ts = t0 + (int64_t)j * T;
+      if (tma) {
+        if (lane == 0) {
+          tma_store_3d(&maps.out, st, c0, (int)ts, b);
+          bulk_commit();
+          bulk_wait_read<0>();  // the copy has read the stage before it is refilled
+        }
+      } else {
+        mbar_wait(&empty[sj], par);  // completes at once: every lane acquires the y writes
+        const int valid = (int)min((int64_t)T, t1 - ts);
+        for (int e = lane; e < T * CH; e += 32) {
+          const int tt = e / CH, c = e - tt * CH;
+          const int64_t ch = (int64_t)c0 + c;
+          if (tt < valid && ch < Dm) {
+            const int64_t gi = ((int64_t)b * L + ts + tt) * Dm + ch;
+            if (ESZ == 2)
+              static_cast<unsigned short*>(p.out)[gi] = *reinterpret_cast<const unsigned short*>(st + 2 * e);
+            else
+              static_cast<uint32_t*>(p.out)[gi] = *reinterpret_cast<const uint32_t*>(st + 4 * e);
+          }
+        }
+        __syncwarp();  // all lanes have read the stage before it is refilled
+      }
+      return true;
+    };
     auto issue = [&](int j) {  // all lanes call; returns false if the stage never freed
       const int sj = j % ST;
-      if (j >= ST) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[sj], ((j / ST) - 1) & 1);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      }
+      if (j >= ST && !release(j - ST)) return false;
       unsigned char* st = stage(j);
       const int ts = (int)(t0 + (int64_t)j * T);
       if (tma) {
@@ -551,7 +592,8 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
         }
       } else {
         // plain loads into the same layout (x / delta / z raw, B / C straight to the
-        // fp32 planes); zero outside the tensor
+        // fp32 planes); zero outside the tensor, except delta past the sequence end,
+        // which is -inf when softplus applies (softplus(-inf) = 0: an identity step)
         const int valid = (int)min((int64_t)T, t1 - (int64_t)ts);
         for (int e = lane; e < T * CH; e += 32) {
           const int tt = e / CH, c = e - tt * CH;
@@ -563,14 +605,15 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
             *reinterpret_cast<unsigned short*>(st + o) =
                 in ? __ldg(static_cast<const unsigned short*>(p.x) + gi) : (unsigned short)0;
             *reinterpret_cast<unsigned short*>(st + XB + o) =
-                in ? __ldg(static_cast<const unsigned short*>(p.delta) + gi) : (unsigned short)0;
+                in ? __ldg(static_cast<const unsigned short*>(p.delta) + gi)
+                   : (unsigned short)(sp ? 0xFF80u : 0u);
             if (gate)
               *reinterpret_cast<unsigned short*>(st + 2 * XB + o) =
                   in ? __ldg(static_cast<const unsigned short*>(p.z) + gi) : (unsigned short)0;
           } else {
             *reinterpret_cast<uint32_t*>(st + o) = in ? __ldg(static_cast<const uint32_t*>(p.x) + gi) : 0u;
             *reinterpret_cast<uint32_t*>(st + XB + o) =
-                in ? __ldg(static_cast<const uint32_t*>(p.delta) + gi) : 0u;
+                in ? __ldg(static_cast<const uint32_t*>(p.delta) + gi) : (sp ? 0xFF800000u : 0u);
             if (gate)
               *reinterpret_cast<uint32_t*>(st + 2 * XB + o) =
                   in ? __ldg(static_cast<const uint32_t*>(p.z) + gi) : 0u;
@@ -615,6 +658,18 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
         }
       }
     };
+    // rows of a TMA tile past the sequence end arrive as zeros; with softplus their
+    // delta becomes -inf, so that the step size there is exactly 0 (an identity step)
+    auto patch_tail = [&](int i) {
+      if (!tma || !sp) return;
+      const int valid = (int)min((int64_t)T, t1 - (t0 + (int64_t)i * T));
+      if (valid >= T) return;
+      unsigned char* dl = stage(i) + XB;
+      for (int e = valid * CH + lane; e < T * CH; e += 32) {
+        if (ESZ == 2) *reinterpret_cast<unsigned short*>(dl + 2 * e) = 0xFF80u;
+        else *reinterpret_cast<uint32_t*>(dl + 4 * e) = 0xFF800000u;
+      }
+    };
     bool ok = true;
     int waited = 0;  // tiles whose arrival this warp has already waited for
     for (int j = 0; j < ST - 1 && j < ntiles && ok; ++j) ok = issue(j);
@@ -628,10 +683,16 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       }
       waited = i + 1;
       widen(i);
+      patch_tail(i);
       __threadfence_block();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ready[i % ST]);
       if (i + ST - 1 < ntiles) ok = issue(i + ST - 1);
+    }
+    if (OUT) {
+      // the last tiles' outputs, as the consumers release them
+      for (int j = released; j < ntiles && ok; ++j) ok = release(j);
+      if (tma && lane == 0) bulk_wait<0>();  // every output copy complete before the CTA leaves
     }
     if (!ok && lane == 0) atomicExch(p.status, kStatusTimeout);
     if (lane == 0 && tma)
@@ -734,26 +795,38 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
   auto run = [&](auto pow_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value && !LTI;
-    int64_t orow = ((int64_t)b * L + t0) * Dm + d;  // out index of step 0 of the tile, this channel
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % ST;
       if (!mbar_wait(&ready[s], (i / ST) & 1)) return false;
-      const unsigned char* st = stage(i);
+      unsigned char* st = stage(i);
       const int64_t ts = t0 + (int64_t)i * T;
       const int nvalid = (int)min((int64_t)T, t1 - ts);
       const float* brow0 = reinterpret_cast<const float*>(st + Gm::OFF_F) + g * S;
 #pragma unroll
       for (int r0 = 0; r0 < T / G; r0 += R) {
-        float xv[R], p1v[R], uv[R];
+        // this lane's step of round r0 + q and its byte offset in an x / delta / z tile
+        auto tq = [&](int q) { return (r0 + q) * G + g; };
+        auto xo = [&](int q) { return (tq(q) * CH + cl) * ESZ; };
+        float xv[R], p1v[R], uv[R], dq[R];
         [[maybe_unused]] float dtv[ZOH ? R : 1];
+        // phase A (the tests of the launch flags are hoisted out of the step loops)
 #pragma unroll
-        for (int q = 0; q < R; ++q) {  // phase A
-          const int tm = (r0 + q) * G + g;
-          const int xo = (tm * CH + cl) * ESZ;
-          xv[q] = IO::lds(st + xo);
-          const float v = IO::lds(st + XB + xo) + biasv;
-          float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
-          if (tm >= nvalid) dt = 0.f;  // past the end: identity step
+        for (int q = 0; q < R; ++q) {
+          xv[q] = IO::lds(st + xo(q));
+          dq[q] = IO::lds(st + XB + xo(q)) + biasv;
+        }
+        if (p.delta_softplus) {
+          // rows past the sequence end hold delta = -inf: step 0, an identity step
+#pragma unroll
+          for (int q = 0; q < R; ++q) dq[q] = softplus<std::is_same<IO, F32>::value>(dq[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < R; ++q)
+            if (tq(q) >= nvalid) dq[q] = 0.f;  // past the end: identity step
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          const float dt = dq[q];
           if constexpr (ZOH) {
             uv[q] = xv[q];
             dtv[q] = dt;
@@ -783,18 +856,21 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
             }
           }
         }
-        if (OUT) {
+        if (OUT) {  // phase C
+          float yq[R];
 #pragma unroll
-          for (int q = 0; q < R; ++q) {  // phase C
-            const int tm = (r0 + q) * G + g;
-            float y = reduce_scatter<G>(yv[q], g);
-            y = fmaf(Dv, xv[q], y);
-            if (gate) y *= silu(IO::lds(st + 2 * XB + (tm * CH + cl) * ESZ));
-            if (valid && tm < nvalid) IO::store(p.out, orow + (int64_t)tm * Dm, y);
+          for (int q = 0; q < R; ++q) yq[q] = fmaf(Dv, xv[q], reduce_scatter<G>(yv[q], g));
+          if (gate) {
+#pragma unroll
+            for (int q = 0; q < R; ++q) yq[q] *= silu(IO::lds(st + 2 * XB + xo(q)));
           }
+          // y takes the place of this lane's x of the same step; the producer copies
+          // the tile to out once the stage is released
+#pragma unroll
+          for (int q = 0; q < R; ++q) IO::sts(st + xo(q), yq[q]);
         }
       }
-      orow += (int64_t)T * Dm;
+      if (OUT) fence_proxy_async_smem();  // y visible to the producer's bulk copy
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }

@@ -393,6 +393,8 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     bool okm = encode3d(&maps.x, x, eb, d.dim, d.seqlen, d.batch, ch, T) &&
                encode3d(&maps.delta, delta, eb, d.dim, d.seqlen, d.batch, ch, T);
     if (okm && z) okm = encode3d(&maps.z, z, eb, d.dim, d.seqlen, d.batch, ch, T);
+    // the output pass writes out in tiles of the x box
+    if (okm) okm = encode3d(&maps.out, out, eb, d.dim, d.seqlen, d.batch, ch, T);
     if (okm && !lti)
       okm = encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T) &&
             encode3d(&maps.C, C, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T);
