@@ -857,17 +857,18 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           }
         }
         if (OUT) {  // phase C
-          float yq[R];
-#pragma unroll
-          for (int q = 0; q < R; ++q) yq[q] = fmaf(Dv, xv[q], reduce_scatter<G>(yv[q], g));
-          if (gate) {
-#pragma unroll
-            for (int q = 0; q < R; ++q) yq[q] *= silu(IO::lds(st + 2 * XB + xo(q)));
-          }
           // y takes the place of this lane's x of the same step; the producer copies
           // the tile to out once the stage is released
+          if (gate) {
 #pragma unroll
-          for (int q = 0; q < R; ++q) IO::sts(st + xo(q), yq[q]);
+            for (int q = 0; q < R; ++q) {
+              const float y = fmaf(Dv, xv[q], reduce_scatter<G>(yv[q], g));
+              IO::sts(st + xo(q), y * silu(IO::lds(st + 2 * XB + xo(q))));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < R; ++q) IO::sts(st + xo(q), fmaf(Dv, xv[q], reduce_scatter<G>(yv[q], g)));
+          }
         }
       }
       if (OUT) fence_proxy_async_smem();  // y visible to the producer's bulk copy
