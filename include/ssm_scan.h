@@ -159,7 +159,7 @@ uint64_t ssm_kernel_launches(void);
 /*
  * Tuning knobs (process-wide, for benchmarks and tests):
  *   "chunks"        force the number of sequence chunks (0 = automatic)
- *   "min_chunk_len" smallest automatic chunk length in steps (default 512)
+ *   "min_chunk_len" smallest automatic chunk length in steps (default 64)
  *   "lanes"         force the lanes per channel G (1, 2 or 4; 0 = automatic).
  *                   Each channel's states are split over G threads.  A G the build
  *                   lacks for this state count makes calls fail with

@@ -790,8 +790,12 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   // overlap instead of running back to back with the state updates:
   //   A  this lane's step of each round: step size, u (and the S4D-real base)
   //   B  the G R steps in order: shuffled step sizes, state updates, C . h shares
-  //   C  reduce-scatter of the shares, D x, gate, store
-  constexpr int R = (G == 1) ? 8 : 4;
+  //   C  reduce-scatter of the shares, D x, gate, y into the stage
+  // More rounds per group give each warp more independent work (the kernels run few
+  // warps per SM): one lane per channel takes a whole tile of up to 16 rounds (not in
+  // the exact-ZOH form, whose extra per-state constants would not fit three CTAs per
+  // SM), two lanes 8, four lanes 4.
+  constexpr int R = (G == 1 && !ZOH) ? (T < 16 ? T : 16) : (G <= 2) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
   auto run = [&](auto pow_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value && !LTI;

@@ -25,7 +25,7 @@ using ssm::ScanParams;
 // ----------------------------------------------------------------- options
 
 std::atomic<int64_t> g_opt_chunks{0};
-std::atomic<int64_t> g_opt_min_chunk_len{512};
+std::atomic<int64_t> g_opt_min_chunk_len{64};
 std::atomic<int64_t> g_opt_lanes{0};
 std::atomic<int64_t> g_opt_lane_threads{32768};
 std::atomic<int64_t> g_opt_ctas_per_sm{3};

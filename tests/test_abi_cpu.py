@@ -110,7 +110,7 @@ def test_options():
         _abi.set_option("chunks", -1)
     for name in ("chunks", "min_chunk_len", "lanes"):
         _abi.set_option(name, 0)
-    _abi.set_option("min_chunk_len", 512)
+    _abi.set_option("min_chunk_len", 64)
     _abi.set_option("lane_threads", 36864)
     _abi.set_option("ctas_per_sm", 3)
     _abi.set_option("inject_stall", 0)
