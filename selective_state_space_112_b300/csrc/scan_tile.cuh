@@ -737,7 +737,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     }
   }
   // S4D-real powers path: every channel of the warp must qualify (a uniform branch)
-  const bool use_pow = !LTI && p.pow_path && __all_sync(0xffffffffu, structured || !valid);
+  const bool use_pow = p.pow_path && __all_sync(0xffffffffu, structured || !valid);
   const float biasv = p.bias ? p.bias[dd] : 0.f;
   const float Dv = p.Dskip ? p.Dskip[dd] : 0.f;
   const float eA0 = p.A[dd * N];
@@ -798,7 +798,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   constexpr int R = (G == 1 && !ZOH) ? (T < 16 ? T : 16) : (G <= 2) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
   auto run = [&](auto pow_tag) -> bool {
-    constexpr bool POW = decltype(pow_tag)::value && !LTI;
+    constexpr bool POW = decltype(pow_tag)::value;
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % ST;
       if (!mbar_wait(&ready[s], (i / ST) & 1)) return false;

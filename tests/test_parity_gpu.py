@@ -117,6 +117,9 @@ EDGE = [
     ("s4d_real_pow", dict(batch=2, seqlen=300, dim=96, dstate=16, a_init="s4d_real"), 2),
     ("lti", dict(batch=2, seqlen=200, dim=40, dstate=16, lti=True, with_bias=False,
                  a_init="random"), 3),
+    # constant coefficients with S4D-real A: the powers path of the LTI kernels
+    ("lti_s4d_pow", dict(batch=2, seqlen=200, dim=40, dstate=16, lti=True, with_bias=False,
+                         a_init="s4d_real"), 3),
     ("D5", dict(batch=4, seqlen=33, dim=5, dstate=4), 0),
 ]
 
