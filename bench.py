@@ -43,10 +43,10 @@ UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDA
 # per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
 # on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (mean of 5 output launches: 256.66 MB read + 60.09 MB write),
+    # long_bf16_16k capture (mean of 5 output launches: 256.71 MB read + 58.67 MB write),
     # scaled by the units processed (x8) to the 131072-step workload
-    "long_bf16": {"bytes_per_launch": 2534000000, "kernel_src_sha": "cf512725049333a9"},
-    "long_bf16_16k": {"bytes_per_launch": 316750000, "kernel_src_sha": "cf512725049333a9"},
+    "long_bf16": {"bytes_per_launch": 2523000000, "kernel_src_sha": "28618117746fe831"},
+    "long_bf16_16k": {"bytes_per_launch": 315380000, "kernel_src_sha": "28618117746fe831"},
 }
 
 
@@ -307,7 +307,8 @@ def main():
     upd_peak = UPDATES_PER_SM_CLK * sms * sm_max * 1e6 / 1e9           # Gupdate/s
     upd_achieved = w.element_updates / (dom_ms * 1e-3) / 1e9
     tr = TRAFFIC.get(args.workload)
-    traffic = tr["bytes_per_launch"] if tr and tr["kernel_src_sha"] == kernel_src_sha() else None
+    traffic = (tr["bytes_per_launch"] if tr and dom == "ssm_scan_output"
+               and tr["kernel_src_sha"] == kernel_src_sha() else None)
     roof = {"bound": "alu", "kernel": dom, "achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
             "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
             "peak_basis": (f"min({EX2_PER_SM_CLK} MUFU ex2, {FMA_LANES_PER_SM_CLK}/{FMA_OPS_PER_UPDATE} FMA lanes)"
