@@ -839,7 +839,18 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
           }
           p1v[q] = dt;
           if (POW) p1v[q] = MFORM ? expm1f(dt * eA0) : ex2(dt * eA0 * kLog2e);
-          if (PASS == 0) kahan_add(S_sum, S_comp, dt);
+        }
+        if (PASS == 0) {
+          // the chunk's step sum: this lane's steps of the group summed pairwise, then
+          // one compensated add (the sum feeds exp(A S) of the carry)
+          float tsum[R];
+#pragma unroll
+          for (int q = 0; q < R; ++q) tsum[q] = dq[q];
+#pragma unroll
+          for (int w = 1; w < R; w *= 2)
+#pragma unroll
+            for (int q = 0; q + w < R; q += 2 * w) tsum[q] += tsum[q + w];
+          kahan_add(S_sum, S_comp, tsum[0]);
         }
         float yv[R][G];
 #pragma unroll
