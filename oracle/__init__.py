@@ -69,6 +69,8 @@ def _load():
             lib.oracle_lti_kernel.argtypes = [pd] * 5 + [i64] * 3 + [i32]
             lib.oracle_causal_conv.restype = i32
             lib.oracle_causal_conv.argtypes = [pd] * 4 + [i64] * 3 + [i32]
+            lib.oracle_conv_silu.restype = i32
+            lib.oracle_conv_silu.argtypes = [pd] * 6 + [i64] * 4 + [i32]
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -134,7 +136,14 @@ def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
     always fp32/fp64 values.
     Returns (out, final_state) as float64 arrays.
     """
-    x64 = widen(x, io_dtype)
+    return _scan64(widen(x, io_dtype), delta, A, B, C, D, z, delta_bias, h0,
+                   delta_softplus=delta_softplus, bbar_mode=bbar_mode,
+                   per_channel_bc=per_channel_bc, io_dtype=io_dtype, threads=threads)
+
+
+def _scan64(x64, delta, A, B, C, D, z, delta_bias, h0, *, delta_softplus, bbar_mode,
+            per_channel_bc, io_dtype, threads):
+    """selective_scan with x already widened to float64."""
     dl64 = widen(delta, io_dtype)
     z64 = widen(z, io_dtype)
     bc_dtype = "f32" if per_channel_bc else io_dtype
@@ -201,6 +210,48 @@ def lti_kernel(A, B, C, dt, L: int, bbar_mode: int = 0):
     if rc != 0:
         raise ValueError("oracle_lti_kernel rejected its arguments")
     return K
+
+
+CONV_WIDTH = 4  # taps of the Mamba block's depthwise causal convolution
+
+
+def conv_silu(x, w, cb=None, hist=None, io_dtype: str = "f32", threads: int = 0):
+    """u = silu(sum_k w[d,k] x[t-k] + cb[d]) with the W-1 inputs before the
+    sequence taken from ``hist`` (batch, dim, W-1), oldest first (zeros when None).
+
+    x: (batch, L, dim) stored as ``io_dtype``; w: (dim, W); cb: (dim,) or None.
+    Returns (u, hist_out) in float64; hist_out holds the last W-1 inputs of the
+    history-extended sequence, oldest first.
+    """
+    x64 = widen(x, io_dtype)
+    w64, cb64 = widen(w), widen(cb)
+    batch, L, dim = x64.shape
+    W = w64.shape[1]
+    assert w64.shape == (dim, W)
+    h64 = None if hist is None else widen(hist)
+    if h64 is not None:
+        assert h64.shape == (batch, dim, W - 1)
+    u = np.empty_like(x64)
+    hout = np.empty((batch, dim, W - 1), dtype=np.float64)
+    rc = _load().oracle_conv_silu(_ptr(x64), _ptr(w64), _ptr(cb64), _ptr(h64), _ptr(u),
+                                  _ptr(hout), batch, L, dim, W, int(threads))
+    if rc != 0:
+        raise ValueError("oracle_conv_silu rejected its arguments")
+    return u, hout
+
+
+def conv_selective_scan(x, conv_w, conv_b, conv_hist, delta, A, B, C, D=None, z=None,
+                        delta_bias=None, h0=None, *, delta_softplus: bool = True,
+                        bbar_mode: int = 0, per_channel_bc: bool = False,
+                        io_dtype: str = "f32", threads: int = 0):
+    """The block prologue followed by the selective scan on its output:
+    u = conv_silu(x, ...), then selective_scan with x := u (the scan input and the
+    D skip both take u).  Returns (out, final_state, conv_hist_out) in float64."""
+    u, hout = conv_silu(x, conv_w, conv_b, conv_hist, io_dtype=io_dtype, threads=threads)
+    out, st = _scan64(u, delta, A, B, C, D, z, delta_bias, h0,
+                      delta_softplus=delta_softplus, bbar_mode=bbar_mode,
+                      per_channel_bc=per_channel_bc, io_dtype=io_dtype, threads=threads)
+    return out, st, hout
 
 
 def causal_conv(x, K, D=None, io_dtype: str = "f32", threads: int = 0):

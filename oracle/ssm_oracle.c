@@ -231,6 +231,54 @@ int oracle_causal_conv(const double* x, const double* K, const double* D,
   return 0;
 }
 
+/*
+ * Prologue of the Mamba block on the branch that feeds the SSM
+ * ("State-space models", section "Mamba: selection", the block description:
+ * a depthwise causal convolution of width 4 and a silu).  Per batch row b and
+ * channel d, with W = width taps (lag k multiplies the input k steps back):
+ *   pre[b,t,d] = sum_{k=0..W-1} w[d,k] * x[b,t-k,d] + cb[d]
+ *   u[b,t,d]   = silu(pre[b,t,d])
+ * Inputs before the sequence (t-k < 0) come from hist[b,d,0..W-2], the W-1
+ * inputs preceding the sequence, oldest first; zero when hist is NULL.
+ * hist_out (may be NULL, may alias hist) receives the last W-1 inputs of the
+ * history-extended sequence, oldest first, for a call that continues it.
+ * cb may be NULL (no bias).  x, u: (batch, seqlen, dim); w: (dim, W).
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_conv_silu(const double* x, const double* w, const double* cb,
+                     const double* hist, double* u, double* hist_out,
+                     int64_t batch, int64_t seqlen, int64_t dim,
+                     int64_t width, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || width < 1 || width > 64) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const int64_t nchan = batch * dim;
+  const int64_t H = width - 1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ch = 0; ch < nchan; ++ch) {
+    const int64_t b = ch / dim;
+    const int64_t d = ch % dim;
+    double past[64];
+    for (int64_t j = 0; j < H; ++j)
+      past[j] = hist ? hist[(b * dim + d) * H + j] : 0.0;
+    /* input at step tau of the history-extended sequence, tau >= -H */
+#define XS(tau) ((tau) < 0 ? past[H + (tau)] : x[(b * seqlen + (tau)) * dim + d])
+    for (int64_t t = 0; t < seqlen; ++t) {
+      double pre = cb ? cb[d] : 0.0;
+      for (int64_t k = 0; k < width; ++k) pre += w[d * width + k] * XS(t - k);
+      u[(b * seqlen + t) * dim + d] = silu(pre);
+    }
+    if (hist_out)
+      for (int64_t j = 0; j < H; ++j)
+        hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j);
+#undef XS
+  }
+  return 0;
+}
+
 /* Number of threads OpenMP would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -33,6 +33,13 @@ MUTANTS = {
     "euler_sign": ("*abar = 1.0 + dt * a;", "*abar = 1.0 - dt * a;"),
     "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     "per_channel_C_row": ("const double* Cv = per_channel_bc ? &C[d * dstate]", "const double* Cv = per_channel_bc ? &C[0]"),
+    "conv_taps_reversed": ("pre += w[d * width + k] * XS(t - k);", "pre += w[d * width + (width - 1 - k)] * XS(t - k);"),
+    "conv_bias_dropped": ("double pre = cb ? cb[d] : 0.0;", "double pre = 0.0;"),
+    "conv_history_reversed": ("past[j] = hist ? hist[(b * dim + d) * H + j] : 0.0;",
+                              "past[j] = hist ? hist[(b * dim + d) * H + (H - 1 - j)] : 0.0;"),
+    "conv_no_silu": ("u[(b * seqlen + t) * dim + d] = silu(pre);", "u[(b * seqlen + t) * dim + d] = pre;"),
+    "conv_hist_out_shift": ("hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j);",
+                            "hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j - 1);"),
 }
 
 

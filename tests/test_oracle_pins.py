@@ -375,3 +375,88 @@ def test_workload_recipe():
     assert back[2] == 1.0078125
     assert np.all(np.abs(back - vals) <= np.abs(vals) * 2.0 ** -8)
     assert np.array_equal(oracle.widen(bits, "bf16"), back.astype(np.float64))
+
+
+# ---------------------------------------------------------- block prologue (conv + silu)
+# "State-space models", section "Mamba: selection", the block description: a depthwise
+# causal convolution of width 4 and a silu on the branch that feeds the SSM.
+
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def test_conv_silu_matches_library_convolution():
+    """pre = numpy's full linear convolution of each channel (the history prepended),
+    truncated causally; u = silu(pre + bias).  hist_out = the last three inputs."""
+    rng = np.random.default_rng(11)
+    batch, L, dim, W = 2, 23, 5, oracle.CONV_WIDTH
+    x = rng.normal(size=(batch, L, dim)).astype(np.float32)
+    w = rng.normal(size=(dim, W)).astype(np.float32)
+    cb = rng.normal(size=dim).astype(np.float32)
+    hist = rng.normal(size=(batch, dim, W - 1)).astype(np.float32)
+    u, hout = oracle.conv_silu(x, w, cb, hist)
+    for b in range(batch):
+        for d in range(dim):
+            ext = np.concatenate([hist[b, d].astype(np.float64), x[b, :, d].astype(np.float64)])
+            pre = np.convolve(ext, w[d].astype(np.float64))[W - 1:W - 1 + L] + cb[d]
+            np.testing.assert_allclose(u[b, :, d], _silu(pre), rtol=1e-13, atol=1e-14)
+            np.testing.assert_array_equal(hout[b, d], ext[-(W - 1):])
+
+
+def test_conv_silu_impulse_response_and_causality():
+    """A unit impulse at step s gives pre = w[d, t - s] for s <= t < s + 4 and 0
+    elsewhere (no bias, zero history): the taps in lag order, nothing before s."""
+    L, dim, W, s = 12, 3, oracle.CONV_WIDTH, 5
+    w = np.array([[0.5, -1.25, 2.0, 0.75], [1.0, 0.0, 0.0, 0.0], [-0.5, 0.25, -0.125, 3.0]])
+    x = np.zeros((1, L, dim))
+    x[0, s, :] = 1.0
+    u, _ = oracle.conv_silu(x, w)
+    for d in range(dim):
+        pre = np.zeros(L)
+        pre[s:s + W] = w[d]
+        np.testing.assert_allclose(u[0, :, d], _silu(pre), rtol=0, atol=1e-15)
+        assert np.all(u[0, :s, d] == 0.0)
+
+
+def test_conv_silu_identity_taps_and_silu_values():
+    """Taps (1, 0, 0, 0) and no bias: u = silu(x).  silu(0) = 0, silu(v) -> v for
+    large v and -> 0 for very negative v; silu(1) = 1 / (1 + 1/e)."""
+    x = np.array([0.0, 1.0, 40.0, -40.0, -1.0]).reshape(1, 5, 1)
+    u, _ = oracle.conv_silu(x, np.array([[1.0, 0.0, 0.0, 0.0]]))
+    assert u[0, 0, 0] == 0.0
+    assert abs(u[0, 1, 0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert abs(u[0, 2, 0] - 40.0) < 1e-15
+    assert 0.0 > u[0, 3, 0] > -1e-15
+    assert abs(u[0, 4, 0] - (-1.0 / (1.0 + math.e))) < 1e-16
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 9])
+def test_conv_silu_history_continuation(split):
+    """Running a sequence in two calls, the second starting from the first call's
+    hist_out, equals one call over the whole sequence (also for a first part
+    shorter than the history, where hist_out still holds older inputs)."""
+    rng = np.random.default_rng(split)
+    batch, L, dim = 2, 14, 4
+    x = rng.normal(size=(batch, L, dim))
+    w = rng.normal(size=(dim, oracle.CONV_WIDTH))
+    cb = rng.normal(size=dim)
+    h0 = rng.normal(size=(batch, dim, oracle.CONV_WIDTH - 1))
+    u_all, h_all = oracle.conv_silu(x, w, cb, h0)
+    u1, h1 = oracle.conv_silu(x[:, :split], w, cb, h0)
+    u2, h2 = oracle.conv_silu(x[:, split:], w, cb, h1)
+    np.testing.assert_array_equal(np.concatenate([u1, u2], axis=1), u_all)
+    np.testing.assert_array_equal(h2, h_all)
+
+
+def test_conv_scan_composes_prologue_and_scan():
+    """The fused-block oracle is the prologue followed by the scan on its output:
+    with taps (1, 0, 0, 0) and no bias it equals the scan of silu(x)."""
+    w = make_workload("cs", batch=2, seqlen=40, dim=6, dstate=4, io="f32", seed=5)
+    taps = np.tile(np.array([[1.0, 0.0, 0.0, 0.0]]), (w.dim, 1))
+    out, st, hout = oracle.conv_selective_scan(
+        w.x, taps, None, None, w.delta, w.A, w.B, w.C, w.D, w.z, w.delta_bias)
+    ref, ref_st = oracle.selective_scan(_silu(w.x.astype(np.float64)), w.delta, w.A, w.B, w.C,
+                                        w.D, w.z, w.delta_bias)
+    np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(st, ref_st, rtol=1e-14, atol=1e-14)
+    np.testing.assert_array_equal(hout, w.x[:, -3:, :].transpose(0, 2, 1).astype(np.float64))
