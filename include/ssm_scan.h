@@ -108,6 +108,38 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
                            float* final_state, const ssm_dims* dims,
                            cudaStream_t stream);
 
+/*
+ * Selective-scan forward with the Mamba-block prologue fused into its load stage
+ * (page "State-space models", section "Mamba: selection", the block description:
+ * a depthwise causal convolution of width 4 and a silu on the branch that feeds the
+ * SSM).  Per batch row b, channel d and step t:
+ *
+ *   u[b,t,d] = silu( sum_{k=0..3} conv_w[d,k] * x[b,t-k,d] + conv_b[d] )
+ *
+ * and the scan of ssm_selective_scan_fwd then runs on u in place of x (both the
+ * input term and the D skip take u).  u is formed in fp32 and never stored.
+ *
+ *   conv_w     : (dim, 4) fp32; tap k multiplies the input k steps back
+ *   conv_b     : (dim) fp32, or NULL (no bias)
+ *   conv_state : (batch, dim, 3) fp32, or NULL.  With dims->state_in it is read
+ *                first as the three inputs before the sequence (x[-3], x[-2],
+ *                x[-1], oldest first; zeros without state_in).  On return (in
+ *                stream order) it holds the last three inputs of the sequence,
+ *                extended by that history when seqlen < 3 (seqlen == 0 keeps it,
+ *                or zero-fills it without state_in).  It must not overlap any
+ *                other tensor.
+ * All other arguments as ssm_selective_scan_fwd.  Built for time-varying B and C
+ * (SSM_BC_TIME_VARYING), bbar_mode 0 and dstate <= 16; other forms return
+ * SSM_ERR_UNSUPPORTED.  A long sequence run in pieces with state_in and both
+ * states carried gives the result of one call over the whole sequence.
+ */
+int ssm_conv_selective_scan_fwd(const void* x, const float* conv_w, const float* conv_b,
+                                float* conv_state, const void* delta, const float* A,
+                                const void* B, const void* C, const float* D,
+                                const void* z, const float* delta_bias, void* out,
+                                float* final_state, const ssm_dims* dims,
+                                cudaStream_t stream);
+
 /* Bytes of the fixed workspace of ssm_selective_scan_fwd_noalloc (16 MiB). */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 

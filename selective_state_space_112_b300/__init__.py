@@ -11,7 +11,8 @@ from . import _abi
 from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, SSM_OK,
                    SSMError, SsmDims)
 
-__all__ = ["ssm_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc", "ssm_check_status", "ssm_status_string",
+__all__ = ["ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc",
+           "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read", "SSMError", "SsmDims"]
 
@@ -39,6 +40,43 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     overwritten with the final state.  Returns ``(out, final_state)``; the
     call is asynchronous on ``stream`` (default: torch's current stream).
     """
+    return _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state, None,
+                 delta_softplus=delta_softplus, state_in=state_in, bbar_mode=bbar_mode,
+                 return_final_state=return_final_state, stream=stream, noalloc=_noalloc)
+
+
+def ssm_conv_selective_scan_fwd(x, conv_w, conv_b, conv_state, delta, A, B, C, D=None, z=None,
+                                delta_bias=None, out=None, final_state=None, *,
+                                delta_softplus: bool = True, state_in: bool = False,
+                                return_final_state: bool = True, stream=None):
+    """Selective-scan forward with the Mamba-block prologue on x:
+    u = silu(sum_k conv_w[d,k] x[t-k] + conv_b[d]) feeds the scan in place of x.
+
+    conv_w: (dim, 4) float32 (tap k multiplies the input k steps back); conv_b: (dim,)
+    float32 or None; conv_state: (batch, dim, 3) float32 or None, read first as the
+    three inputs before the sequence when ``state_in`` and overwritten with the last
+    three inputs.  Other arguments as ``ssm_selective_scan_fwd`` (time-varying B, C).
+    Returns ``(out, final_state)``.
+    """
+    torch = _torch()
+    dim = x.shape[-1]
+    for name, t, shp in (("conv_w", conv_w, (dim, 4)), ("conv_b", conv_b, (dim,)),
+                         ("conv_state", conv_state, (x.shape[0], dim, 3))):
+        if t is None:
+            continue
+        if t.dtype != torch.float32 or tuple(t.shape) != shp:
+            raise ValueError(f"{name}: expected float32 {shp}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if conv_w is None:
+        raise ValueError("conv_w is required")
+    return _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state,
+                 (conv_w, conv_b, conv_state), delta_softplus=delta_softplus, state_in=state_in,
+                 bbar_mode=0, return_final_state=return_final_state, stream=stream, noalloc=False)
+
+
+def _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state, conv, *, delta_softplus,
+          state_in, bbar_mode, return_final_state, stream, noalloc):
     torch = _torch()
     if x.dtype == torch.float32:
         io = SSM_F32
@@ -79,11 +117,19 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         stream = torch.cuda.current_stream(x.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    rc = _abi.call_fwd(_addr(x), _addr(delta), _addr(A), _addr(B), _addr(C), _addr(D),
-                       _addr(z), _addr(delta_bias), _addr(out), _addr(final_state), dims,
-                       int(stream), noalloc=_noalloc)
+    if conv is not None:
+        cw, cb, cs = conv
+        rc = _abi.call_conv_fwd(_addr(x), _addr(cw), _addr(cb), _addr(cs), _addr(delta), _addr(A),
+                                _addr(B), _addr(C), _addr(D), _addr(z), _addr(delta_bias),
+                                _addr(out), _addr(final_state), dims, int(stream))
+        what = "ssm_conv_selective_scan_fwd"
+    else:
+        rc = _abi.call_fwd(_addr(x), _addr(delta), _addr(A), _addr(B), _addr(C), _addr(D),
+                           _addr(z), _addr(delta_bias), _addr(out), _addr(final_state), dims,
+                           int(stream), noalloc=noalloc)
+        what = "ssm_selective_scan_fwd_noalloc" if noalloc else "ssm_selective_scan_fwd"
     if rc != SSM_OK:
-        raise SSMError(rc, "ssm_selective_scan_fwd_noalloc" if _noalloc else "ssm_selective_scan_fwd")
+        raise SSMError(rc, what)
     return out, final_state
 
 

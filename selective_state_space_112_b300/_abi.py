@@ -25,7 +25,8 @@ SSM_OK = 0
 SSM_ERR_SCRATCH = -10
 SSM_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/ssm_scan.h
 # names as declared in include/ssm_scan.h
-EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc", "ssm_check_status", "ssm_status_string",
+EXPORTS = ("ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc",
+           "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read")
 
@@ -64,6 +65,8 @@ def lib():
             vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             L.ssm_selective_scan_fwd.restype = i32
             L.ssm_selective_scan_fwd.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
+            L.ssm_conv_selective_scan_fwd.restype = i32
+            L.ssm_conv_selective_scan_fwd.argtypes = [vp] * 13 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_selective_scan_fwd_noalloc.restype = i32
             L.ssm_selective_scan_fwd_noalloc.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_check_status.restype = i32
@@ -98,6 +101,15 @@ def call_fwd(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims: SsmDim
     return fn(x or None, delta or None, A or None, B or None, C or None, D or None,
               z or None, delta_bias or None, out or None, final_state or None,
               ctypes.byref(dims), stream or None)
+
+
+def call_conv_fwd(x, conv_w, conv_b, conv_state, delta, A, B, C, D, z, delta_bias, out,
+                  final_state, dims: SsmDims, stream) -> int:
+    """Raw call of ssm_conv_selective_scan_fwd (integer addresses, 0 = NULL)."""
+    return lib().ssm_conv_selective_scan_fwd(
+        x or None, conv_w or None, conv_b or None, conv_state or None, delta or None, A or None,
+        B or None, C or None, D or None, z or None, delta_bias or None, out or None,
+        final_state or None, ctypes.byref(dims), stream or None)
 
 
 def check_status(stream=0) -> int:

@@ -1,7 +1,7 @@
 // Kernel lookup for the tiled selective-scan kernel: one entry per (io dtype, B/C
 // layout, input-term form, pass, states per lane S, lanes per channel G).  The
-// instantiations are spread over eight translation units
-// (kernels_<io>_<layout>[_zoh].cu) so that they build in parallel.
+// instantiations are spread over ten translation units
+// (kernels_<io>_<layout>[_zoh|_conv].cu) so that they build in parallel.
 #pragma once
 
 #include "scan_tile.cuh"
@@ -24,11 +24,11 @@ struct KernelInfo {
   X(2, 1) X(4, 1) X(2, 2) X(8, 1) X(4, 2) X(2, 4) X(16, 1) X(8, 2) X(4, 4) \
   X(16, 2) X(8, 4) X(16, 4)
 
-template <typename IO, int S, int G, bool LTI, int PASS, bool ZOH>
+template <typename IO, int S, int G, bool LTI, int PASS, int VAR>
 KernelInfo kernel_info() {
   using Gm = Geo<IO, S, G>;
   KernelInfo k;
-  k.fn = scan_tile_kernel<IO, S, G, LTI, PASS, ZOH>;
+  k.fn = scan_tile_kernel<IO, S, G, LTI, PASS, VAR>;
   k.nt = Gm::NT;
   k.ch = Gm::CH;
   k.t = Gm::T;
@@ -36,18 +36,21 @@ KernelInfo kernel_info() {
   return k;
 }
 
-template <typename IO, bool LTI, int PASS, bool ZOH>
+template <typename IO, bool LTI, int PASS, int VAR>
 KernelInfo pick_sg(int S, int G) {
-#define SSM_CASE(s_, g_) \
-  if (S == s_ && G == g_) return kernel_info<IO, s_, g_, LTI, PASS, ZOH>();
+  // the prologue form (VAR 2) is built for one lane per channel only
+#define SSM_CASE(s_, g_)                                        \
+  if constexpr (VAR != 2 || g_ == 1) {                          \
+    if (S == s_ && G == g_) return kernel_info<IO, s_, g_, LTI, PASS, VAR>(); \
+  }
   SSM_FOR_EACH_SG(SSM_CASE)
 #undef SSM_CASE
   return KernelInfo();
 }
 
-template <typename IO, bool LTI, bool ZOH>
+template <typename IO, bool LTI, int VAR>
 KernelInfo lookup_impl(int S, int G, int pass) {
-  return pass ? pick_sg<IO, LTI, 1, ZOH>(S, G) : pick_sg<IO, LTI, 0, ZOH>(S, G);
+  return pass ? pick_sg<IO, LTI, 1, VAR>(S, G) : pick_sg<IO, LTI, 0, VAR>(S, G);
 }
 
 // Defined in kernels_<io>_<layout>[_zoh].cu.
@@ -59,9 +62,11 @@ KernelInfo lookup_f32_tv_zoh(int S, int G, int pass);
 KernelInfo lookup_f32_lti_zoh(int S, int G, int pass);
 KernelInfo lookup_bf16_tv_zoh(int S, int G, int pass);
 KernelInfo lookup_bf16_lti_zoh(int S, int G, int pass);
+KernelInfo lookup_f32_tv_conv(int S, int G, int pass);
+KernelInfo lookup_bf16_tv_conv(int S, int G, int pass);
 
 // Recurrent step kernel (sequence length 1), step_kernel.cu: G threads per channel of
 // 4 states each, G in {1, 2, 4, 8, 16}.
-KernelInfo lookup_step(int io_bf16, bool lti, int G);
+KernelInfo lookup_step(int io_bf16, bool lti, int G, bool conv);
 
 }  // namespace ssm

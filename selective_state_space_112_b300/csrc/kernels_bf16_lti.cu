@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_bf16_lti(int S, int G, int pass) { return lookup_impl<BF16, true, false>(S, G, pass); }
+KernelInfo lookup_bf16_lti(int S, int G, int pass) { return lookup_impl<BF16, true, 0>(S, G, pass); }
 }  // namespace ssm

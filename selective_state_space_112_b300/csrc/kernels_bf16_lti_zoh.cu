@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_bf16_lti_zoh(int S, int G, int pass) { return lookup_impl<BF16, true, true>(S, G, pass); }
+KernelInfo lookup_bf16_lti_zoh(int S, int G, int pass) { return lookup_impl<BF16, true, 1>(S, G, pass); }
 }  // namespace ssm

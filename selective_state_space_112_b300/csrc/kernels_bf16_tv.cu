@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_bf16_tv(int S, int G, int pass) { return lookup_impl<BF16, false, false>(S, G, pass); }
+KernelInfo lookup_bf16_tv(int S, int G, int pass) { return lookup_impl<BF16, false, 0>(S, G, pass); }
 }  // namespace ssm

@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_bf16_tv_zoh(int S, int G, int pass) { return lookup_impl<BF16, false, true>(S, G, pass); }
+KernelInfo lookup_bf16_tv_zoh(int S, int G, int pass) { return lookup_impl<BF16, false, 1>(S, G, pass); }
 }  // namespace ssm

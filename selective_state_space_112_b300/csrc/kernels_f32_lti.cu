@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_f32_lti(int S, int G, int pass) { return lookup_impl<F32, true, false>(S, G, pass); }
+KernelInfo lookup_f32_lti(int S, int G, int pass) { return lookup_impl<F32, true, 0>(S, G, pass); }
 }  // namespace ssm

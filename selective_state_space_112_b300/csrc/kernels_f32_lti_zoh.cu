@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_f32_lti_zoh(int S, int G, int pass) { return lookup_impl<F32, true, true>(S, G, pass); }
+KernelInfo lookup_f32_lti_zoh(int S, int G, int pass) { return lookup_impl<F32, true, 1>(S, G, pass); }
 }  // namespace ssm

@@ -2,5 +2,5 @@
 #include "kernel_table.cuh"
 
 namespace ssm {
-KernelInfo lookup_f32_tv(int S, int G, int pass) { return lookup_impl<F32, false, false>(S, G, pass); }
+KernelInfo lookup_f32_tv(int S, int G, int pass) { return lookup_impl<F32, false, 0>(S, G, pass); }
 }  // namespace ssm

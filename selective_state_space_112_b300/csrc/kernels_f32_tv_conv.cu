@@ -1,0 +1,6 @@
+// Instantiations of the tiled selective-scan kernel: fp32 inputs, time-varying B and C, the Mamba-block prologue (causal conv of width 4 + silu on x), one lane per channel.
+#include "kernel_table.cuh"
+
+namespace ssm {
+KernelInfo lookup_f32_tv_conv(int S, int G, int pass) { return lookup_impl<F32, false, 2>(S, G, pass); }
+}  // namespace ssm

@@ -53,5 +53,5 @@ extern "C" int ssm_selective_scan_fwd_noalloc(const void* x, const void* delta, 
   // Nothing in the scratch has to start at zero: the aggregate pass writes every entry
   // that the output pass of the same call reads.
   return ssm_internal::scan_forward(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims, stream,
-                                    scratch, SSM_NOALLOC_SCRATCH_BYTES);
+                                    scratch, SSM_NOALLOC_SCRATCH_BYTES, nullptr);
 }

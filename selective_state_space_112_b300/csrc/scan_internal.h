@@ -9,10 +9,20 @@ namespace ssm_internal {
 
 // Runs one selective-scan call.  With scratch == nullptr the chunk-carry workspace
 // comes from the library's memory pool; otherwise it is taken from the caller's
-// scratch_bytes of device memory at `scratch` and nothing is allocated.
+// scratch_bytes of device memory at `scratch` and nothing is allocated.  conv: the
+// block prologue on x, or null.
+// The Mamba-block prologue applied to x before the scan: taps (dim, 4), bias (dim)
+// or null, and the (batch, dim, 3) input history (read with dims->state_in, written
+// when not null).
+struct ConvPrologue {
+  const float* w;
+  const float* b;
+  float* state;
+};
+
 int scan_forward(const void* x, const void* delta, const float* A, const void* B, const void* C,
                  const float* D, const void* z, const float* delta_bias, void* out,
                  float* final_state, const ssm_dims* dims, cudaStream_t stream, void* scratch,
-                 size_t scratch_bytes);
+                 size_t scratch_bytes, const ConvPrologue* conv);
 
 }  // namespace ssm_internal

@@ -92,6 +92,13 @@ struct ScanParams {
   int bbar_mode;        // 0: Bbar = step B; 1: exact ZOH, Bbar = (exp(step A) - 1) / A B
   int stall_tile;       // failure injection for tests: the producer stops before this
                         // tile and never hands it over (-1: off)
+  // block prologue (variant 2): u = silu(sum_k conv_w[d,k] x[t-k] + conv_b[d]) feeds the
+  // scan in place of x
+  const float* conv_w;        // (dim, 4), lag k multiplies the input k steps back
+  const float* conv_b;        // (dim) or null
+  const float* conv_hist_in;  // (batch, dim, 3) inputs before the sequence, oldest first; null: zeros
+  float* conv_state_out;      // (batch, dim, 3) last three inputs, oldest first; null: not written
+  float* ws_cs;               // copy of conv_hist_in for the output pass when nchunks > 1
 };
 
 struct TmaMaps {
@@ -484,9 +491,11 @@ __device__ __forceinline__ float reduce_scatter(const float (&v)[G], int g) {
 // PASS 0: chunk aggregate (end state from a zero start, sum of steps) of chunks
 //         0 .. nchunks-2.
 // PASS 1: output pass (carry-in, out, final state).
-// ZOH: exact zero-order-hold input term (bbar_mode 1), a separate instantiation so
-// that the common path carries none of its registers.
-template <typename IO, int S, int G, bool LTI, int PASS, bool ZOH>
+// VAR 0: the scan as stated; VAR 1: exact zero-order-hold input term (bbar_mode 1);
+// VAR 2: the Mamba-block prologue (depthwise causal conv of width 4 + silu on x),
+// one lane per channel.  Separate instantiations, so that the common path carries
+// none of the other forms' registers.
+template <typename IO, int S, int G, bool LTI, int PASS, int VAR>
 __global__ void __launch_bounds__(Geo<IO, S, G>::NT)
 scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   using Gm = Geo<IO, S, G>;
@@ -494,6 +503,8 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   constexpr int ESZ = Gm::ESZ, XB = Gm::XB, BB = Gm::BB;
   constexpr bool OUT = (PASS == 1);
   constexpr bool MFORM = LTI || !IO::kFastDecay;
+  constexpr bool ZOH = (VAR == 1), CONV = (VAR == 2);
+  static_assert(!CONV || G == 1, "the prologue runs one lane per channel");
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::OFF_BAR);  // raw tile landed (TMA)
   uint64_t* ready = full + ST;                                         // fp32 B / C planes written
@@ -782,6 +793,32 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     for (int i = 0; i < S / 2; ++i) h[i] = f2(hv[2 * i], hv[2 * i + 1]);
   }
 
+  // block prologue: taps, bias and the window of the three raw inputs before the
+  // next step (xw0 oldest); a chunk after the first starts from the inputs before it
+  [[maybe_unused]] float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
+  [[maybe_unused]] float cbv = 0.f, xw0 = 0.f, xw1 = 0.f, xw2 = 0.f;
+  if constexpr (CONV) {
+    cw = *reinterpret_cast<const float4*>(p.conv_w + dd * 4);
+    cbv = p.conv_b ? p.conv_b[dd] : 0.f;
+    if (t0 > 0) {
+      const int64_t xi = ((int64_t)b * L + t0 - 3) * Dm + dd;
+      xw0 = IO::load(p.x, xi);
+      xw1 = IO::load(p.x, xi + Dm);
+      xw2 = IO::load(p.x, xi + 2 * Dm);
+    } else if (p.conv_hist_in) {
+      const float* src = (PASS == 1 && p.ws_cs) ? p.ws_cs : p.conv_hist_in;
+      const int64_t ci3 = ((int64_t)b * Dm + dd) * 3;
+      xw0 = src[ci3];
+      xw1 = src[ci3 + 1];
+      xw2 = src[ci3 + 2];
+      if (PASS == 0 && p.ws_cs && valid) {
+        p.ws_cs[ci3] = xw0;
+        p.ws_cs[ci3 + 1] = xw1;
+        p.ws_cs[ci3 + 2] = xw2;
+      }
+    }
+  }
+
   float S_sum = 0.f, S_comp = 0.f;  // PASS 0: this lane's share of the chunk's step sum
   const int gbase = lane & ~(G - 1);
 
@@ -793,9 +830,9 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   //   C  reduce-scatter of the shares, D x, gate, y into the stage
   // More rounds per group give each warp more independent work (the kernels run few
   // warps per SM): one lane per channel takes a whole tile of up to 16 rounds (not in
-  // the exact-ZOH form, whose extra per-state constants would not fit three CTAs per
-  // SM), two lanes 8, four lanes 4.
-  constexpr int R = (G == 1 && !ZOH) ? (T < 16 ? T : 16) : (G <= 2) ? 8 : 4;
+  // the exact-ZOH and prologue forms, whose extra per-lane values would not fit three
+  // CTAs per SM), two lanes 8, four lanes 4.
+  constexpr int R = (G == 1 && VAR == 0) ? (T < 16 ? T : 16) : (G <= 2) ? 8 : 4;
   static_assert((T / G) % R == 0, "whole groups of rounds per tile");
   auto run = [&](auto pow_tag) -> bool {
     constexpr bool POW = decltype(pow_tag)::value;
@@ -818,6 +855,23 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
         for (int q = 0; q < R; ++q) {
           xv[q] = IO::lds(st + xo(q));
           dq[q] = IO::lds(st + XB + xo(q)) + biasv;
+        }
+        if constexpr (CONV) {
+          // u_t = silu(w0 x_t + w1 x_{t-1} + w2 x_{t-2} + w3 x_{t-3} + b): the scan and
+          // the D skip take u; the window keeps the group's last three raw inputs
+          float ext[R + 3];
+          ext[0] = xw0;
+          ext[1] = xw1;
+          ext[2] = xw2;
+#pragma unroll
+          for (int q = 0; q < R; ++q) ext[q + 3] = xv[q];
+          xw0 = ext[R];
+          xw1 = ext[R + 1];
+          xw2 = ext[R + 2];
+#pragma unroll
+          for (int q = 0; q < R; ++q)
+            xv[q] = silu(fmaf(cw.x, ext[q + 3], fmaf(cw.y, ext[q + 2], fmaf(cw.z, ext[q + 1],
+                                                                            fmaf(cw.w, ext[q], cbv)))));
         }
         if (p.delta_softplus) {
           // rows past the sequence end hold delta = -inf: step 0, an identity step
@@ -900,6 +954,21 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
 
   // ---- results
   if (PASS == 1) {
+    if (CONV && chunk == p.nchunks - 1 && p.conv_state_out && valid) {
+      // the last three raw inputs of the history-extended sequence, oldest first (a
+      // sequence shorter than three keeps part of the history; then there is one
+      // chunk, and this lane read that history itself)
+      float v[3];
+      const int64_t ci3 = ((int64_t)b * Dm + d) * 3;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int64_t tau = L - 3 + j;
+        v[j] = tau >= 0 ? IO::load(p.x, ((int64_t)b * L + tau) * Dm + d)
+                        : (p.conv_hist_in ? p.conv_hist_in[ci3 + 3 + tau] : 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 3; ++j) p.conv_state_out[ci3 + j] = v[j];
+    }
     if (chunk == p.nchunks - 1 && p.final_state && valid) {
       const int64_t sidx = ((int64_t)b * Dm + d) * N;
 #pragma unroll

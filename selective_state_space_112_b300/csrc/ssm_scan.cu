@@ -84,8 +84,13 @@ struct Plan {
   ssm::KernelInfo out_k, agg_k;
 };
 
-ssm::KernelInfo lookup(int io, bool lti, int S, int G, int pass, bool zoh) {
-  if (zoh) {
+// var 0: the scan as stated; 1: exact ZOH input term; 2: block prologue (conv + silu).
+ssm::KernelInfo lookup(int io, bool lti, int S, int G, int pass, int var) {
+  if (var == 2) {
+    if (lti) return ssm::KernelInfo();
+    return io == SSM_F32 ? ssm::lookup_f32_tv_conv(S, G, pass) : ssm::lookup_bf16_tv_conv(S, G, pass);
+  }
+  if (var == 1) {
     if (io == SSM_F32) return lti ? ssm::lookup_f32_lti_zoh(S, G, pass) : ssm::lookup_f32_tv_zoh(S, G, pass);
     return lti ? ssm::lookup_bf16_lti_zoh(S, G, pass) : ssm::lookup_bf16_tv_zoh(S, G, pass);
   }
@@ -153,13 +158,13 @@ int occupancy(const ssm::KernelInfo& k) {
 // SM: every chunk but the last is then scanned twice (aggregate, output), so the
 // chunk count is the largest that still fits ctas_per_sm CTAs on every SM (one
 // wave, evenly spread).
-bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
+bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl) {
   const int ns = padded_states(d.dstate);
   const bool lti = d.bc_layout == SSM_BC_PER_CHANNEL;
   std::vector<int> cand;
   for (int G = 1; G <= 4; G *= 2) {
     const int S = ns / G;
-    if (S >= 2 && S <= 16 && lookup(d.io_dtype, lti, S, G, 1, false).fn) cand.push_back(G);
+    if (S >= 2 && S <= 16 && lookup(d.io_dtype, lti, S, G, 1, conv ? 2 : 0).fn) cand.push_back(G);
   }
   if (cand.empty()) return false;
   const int64_t forced = g_opt_lanes.load();
@@ -184,8 +189,9 @@ bool make_plan(const ssm_dims& d, int sms, Plan* pl) {
   }
   pl->G = G;
   pl->S = ns / G;
-  pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1, d.bbar_mode == 1);
-  pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0, d.bbar_mode == 1);
+  const int var = conv ? 2 : d.bbar_mode;
+  pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1, var);
+  pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0, var);
   pl->tma = g_opt_tma.load() && tma_ok(d);
   int64_t k = g_opt_chunks.load();
   if (k <= 0) {
@@ -301,7 +307,7 @@ namespace ssm_internal {
 int scan_forward(const void* x, const void* delta, const float* A, const void* B, const void* C,
                  const float* D, const void* z, const float* delta_bias, void* out,
                  float* final_state, const ssm_dims* dims, cudaStream_t stream, void* scratch,
-                 size_t scratch_bytes) {
+                 size_t scratch_bytes, const ConvPrologue* conv) {
   if (!dims) return SSM_ERR_NULL;
   const ssm_dims d = *dims;
   if (d.batch <= 0 || d.dim <= 0 || d.dstate <= 0 || d.dstate > 64 || d.seqlen < 0)
@@ -316,6 +322,18 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   const void* ptrs[] = {x, delta, A, B, C, D, z, delta_bias, out, final_state};
   for (const void* q : ptrs)
     if (q && ((uintptr_t)q & 15u)) return SSM_ERR_ALIGN;
+  if (conv) {
+    if (!conv->w) return SSM_ERR_NULL;
+    const void* cptrs[] = {conv->w, conv->b, conv->state};
+    for (const void* q : cptrs)
+      if (q && ((uintptr_t)q & 15u)) return SSM_ERR_ALIGN;
+    // the prologue form: time-varying B and C, the fused scan's input term, one lane
+    // per channel (N <= 16)
+    if (d.bc_layout != SSM_BC_TIME_VARYING || d.bbar_mode != 0 || d.dstate > 16)
+      return SSM_ERR_UNSUPPORTED;
+  }
+  float* const cstate = conv ? conv->state : nullptr;
+  const float* const chist = (conv && d.state_in) ? conv->state : nullptr;
 
   const size_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
   const size_t act = (size_t)d.batch * d.seqlen * d.dim * esz;
@@ -330,10 +348,20 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     if (overlaps(final_state, st, in.p, in.n)) return SSM_ERR_OVERLAP;
   }
   if (overlaps(final_state, st, out, act)) return SSM_ERR_OVERLAP;
+  const size_t cst = (size_t)d.batch * d.dim * 3 * 4;
+  if (cstate) {
+    for (auto& in : ins)
+      if (overlaps(cstate, cst, in.p, in.n)) return SSM_ERR_OVERLAP;
+    if (overlaps(cstate, cst, out, act) || overlaps(cstate, cst, final_state, st) ||
+        overlaps(cstate, cst, conv->w, (size_t)d.dim * 16) || overlaps(cstate, cst, conv->b, (size_t)d.dim * 4))
+      return SSM_ERR_OVERLAP;
+  }
 
   if (d.seqlen == 0) {
     if (final_state && !d.state_in &&
         cudaMemsetAsync(final_state, 0, st, stream) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    if (cstate && !d.state_in && cudaMemsetAsync(cstate, 0, cst, stream) != cudaSuccess)
       return SSM_ERR_CUDA;
     return SSM_OK;
   }
@@ -346,9 +374,13 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     int ns = 4;
     while (ns < d.dstate) ns *= 2;
     const int G = ns / 4;
-    const ssm::KernelInfo k = ssm::lookup_step(d.io_dtype == SSM_BF16, lti, G);
+    const ssm::KernelInfo k = ssm::lookup_step(d.io_dtype == SSM_BF16, lti, G, conv != nullptr);
+    if (!k.fn) return SSM_ERR_UNSUPPORTED;
     ScanParams p;
     std::memset(&p, 0, sizeof p);
+    if (conv) {
+      p.conv_w = conv->w; p.conv_b = conv->b; p.conv_hist_in = chist; p.conv_state_out = cstate;
+    }
     p.x = x; p.delta = delta; p.z = z; p.out = out; p.A = A; p.B = B; p.C = C;
     p.Dskip = D; p.bias = delta_bias; p.final_state = final_state;
     p.h_init = d.state_in ? final_state : nullptr;
@@ -365,7 +397,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SSM_ERR_CUDA;
   if (d.batch > 65535) return SSM_ERR_DIMS;
   Plan pl;
-  if (!make_plan(d, sms, &pl)) return SSM_ERR_UNSUPPORTED;
+  if (!make_plan(d, sms, conv != nullptr, &pl)) return SSM_ERR_UNSUPPORTED;
 
   ScanParams p;
   std::memset(&p, 0, sizeof p);
@@ -379,6 +411,9 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   p.use_tma = pl.tma ? 1 : 0;
   p.bbar_mode = d.bbar_mode;
   p.stall_tile = (int)g_opt_inject_stall.load() - 1;
+  if (conv) {
+    p.conv_w = conv->w; p.conv_b = conv->b; p.conv_hist_in = chist; p.conv_state_out = cstate;
+  }
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
   p.status = status;
@@ -406,7 +441,10 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     const size_t nH = (size_t)(pl.nchunks - 1) * d.batch * d.dim * d.dstate;
     const size_t nS = (size_t)(pl.nchunks - 1) * d.batch * d.dim;
     const size_t nh0 = d.state_in ? (size_t)d.batch * d.dim * d.dstate : 0;
-    const size_t bytes = (nH + nS + nh0) * sizeof(float);
+    // the prologue's input history, copied by the aggregate pass: the output pass
+    // writes the new history over the same buffer
+    const size_t ncs = chist ? (size_t)d.batch * d.dim * 3 : 0;
+    const size_t bytes = (nH + nS + nh0 + ncs) * sizeof(float);
     if (scratch) {
       if (bytes > scratch_bytes) return SSM_ERR_SCRATCH;
       p.ws_H = static_cast<float*>(scratch);
@@ -418,6 +456,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     }
     p.ws_S = p.ws_H + nH;
     p.ws_h0 = nh0 ? p.ws_S + nS : nullptr;
+    p.ws_cs = ncs ? p.ws_S + nS + nh0 : nullptr;
     int rc = launch(pl.agg_k, 0, dim3(gx, (unsigned)(pl.nchunks - 1), (unsigned)d.batch), maps, p, stream);
     if (rc != SSM_OK) {
       if (ws) cudaFreeAsync(ws, stream);
@@ -438,7 +477,17 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
                            const float* delta_bias, void* out, float* final_state,
                            const ssm_dims* dims, cudaStream_t stream) {
   return ssm_internal::scan_forward(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims, stream,
-                                    nullptr, 0);
+                                    nullptr, 0, nullptr);
+}
+
+int ssm_conv_selective_scan_fwd(const void* x, const float* conv_w, const float* conv_b,
+                                float* conv_state, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, void* out, float* final_state,
+                                const ssm_dims* dims, cudaStream_t stream) {
+  const ssm_internal::ConvPrologue cp{conv_w, conv_b, conv_state};
+  return ssm_internal::scan_forward(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims, stream,
+                                    nullptr, 0, &cp);
 }
 
 int ssm_check_status(cudaStream_t stream) {

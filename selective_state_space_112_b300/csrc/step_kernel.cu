@@ -9,14 +9,16 @@
 // state moved as one 16-byte vector per thread (G = padded N / 4 consecutive threads
 // per channel, whole 64-byte rows per channel for N = 16).  Each thread forms the
 // channel's step size itself (G-fold redundant scalar work, free next to the state
-// traffic), and the G shares of C . h meet by warp shuffles.
+// traffic), and the G shares of C . h meet by warp shuffles.  With the Mamba-block
+// prologue (CONV) the input is u = silu(w0 x + w1 x_{-1} + w2 x_{-2} + w3 x_{-3} + b)
+// from the stored three-input history, which the channel's first thread then shifts.
 #include <cuda_runtime.h>
 
 #include "kernel_table.cuh"
 
 namespace ssm {
 
-template <typename IO, int G, bool LTI>
+template <typename IO, int G, bool LTI, bool CONV>
 __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMaps, const ScanParams p) {
   constexpr bool MFORM = LTI || !IO::kFastDecay;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -28,7 +30,17 @@ __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMa
   const int64_t cc = valid ? ch : 0;
   const int64_t b = cc / Dm, d = cc - b * Dm;
 
-  const float xv = IO::load(p.x, cc);  // x[b, 0, d]: (batch, 1, dim) is row-major (batch, dim)
+  float xv = IO::load(p.x, cc);  // x[b, 0, d]: (batch, 1, dim) is row-major (batch, dim)
+  [[maybe_unused]] float hist[3] = {0.f, 0.f, 0.f};  // x_{-3}, x_{-2}, x_{-1}
+  const float x_raw = xv;
+  if (CONV) {
+    if (p.conv_hist_in)
+      for (int j = 0; j < 3; ++j) hist[j] = p.conv_hist_in[cc * 3 + j];
+    const float4 w = *reinterpret_cast<const float4*>(p.conv_w + d * 4);
+    const float pre = fmaf(w.x, x_raw, fmaf(w.y, hist[2], fmaf(w.z, hist[1], fmaf(w.w, hist[0],
+                                                                               p.conv_b ? p.conv_b[d] : 0.f))));
+    xv = silu(pre);
+  }
   const float v = IO::load(p.delta, cc) + (p.bias ? p.bias[d] : 0.f);
   const float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
 
@@ -74,8 +86,14 @@ __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMa
   }
 #pragma unroll
   for (int off = 1; off < G; off <<= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+  if (CONV) __syncwarp();  // every thread has read the history before it is shifted
 
   if (!valid) return;
+  if (CONV && g == 0 && p.conv_state_out) {
+    p.conv_state_out[cc * 3] = hist[1];
+    p.conv_state_out[cc * 3 + 1] = hist[2];
+    p.conv_state_out[cc * 3 + 2] = x_raw;
+  }
   if (p.final_state) {
     if (vec) {
       *reinterpret_cast<float4*>(p.final_state + srow + n0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
@@ -92,15 +110,15 @@ __global__ void __launch_bounds__(256) step_kernel(const __grid_constant__ TmaMa
   }
 }
 
-template <typename IO, bool LTI>
+template <typename IO, bool LTI, bool CONV>
 KernelInfo step_info(int G) {
   KernelInfo k;
   switch (G) {
-    case 1: k.fn = step_kernel<IO, 1, LTI>; break;
-    case 2: k.fn = step_kernel<IO, 2, LTI>; break;
-    case 4: k.fn = step_kernel<IO, 4, LTI>; break;
-    case 8: k.fn = step_kernel<IO, 8, LTI>; break;
-    case 16: k.fn = step_kernel<IO, 16, LTI>; break;
+    case 1: k.fn = step_kernel<IO, 1, LTI, CONV>; break;
+    case 2: k.fn = step_kernel<IO, 2, LTI, CONV>; break;
+    case 4: k.fn = step_kernel<IO, 4, LTI, CONV>; break;
+    case 8: k.fn = step_kernel<IO, 8, LTI, CONV>; break;
+    case 16: k.fn = step_kernel<IO, 16, LTI, CONV>; break;
     default: return k;
   }
   k.nt = 256;
@@ -110,9 +128,13 @@ KernelInfo step_info(int G) {
   return k;
 }
 
-KernelInfo lookup_step(int io_bf16, bool lti, int G) {
-  if (io_bf16) return lti ? step_info<BF16, true>(G) : step_info<BF16, false>(G);
-  return lti ? step_info<F32, true>(G) : step_info<F32, false>(G);
+KernelInfo lookup_step(int io_bf16, bool lti, int G, bool conv) {
+  if (conv) {  // the prologue form: time-varying B and C
+    if (lti) return KernelInfo();
+    return io_bf16 ? step_info<BF16, false, true>(G) : step_info<F32, false, true>(G);
+  }
+  if (io_bf16) return lti ? step_info<BF16, true, false>(G) : step_info<BF16, false, false>(G);
+  return lti ? step_info<F32, true, false>(G) : step_info<F32, false, false>(G);
 }
 
 }  // namespace ssm

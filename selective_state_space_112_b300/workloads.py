@@ -14,6 +14,10 @@ Recipe (shapes of Mamba layers; no trained weights, no dataset):
                ~ N(0, variance 1/N) per (d, n) for the LTI workload
   D            ~ N(0, 1) per channel
   h_init       ~ N(0, 1) per (b, d, n) for the recurrent step workload
+Block prologue (``make_conv``, its own generator seeded with seed + 7919):
+  conv taps    ~ U[-1/2, 1/2] per (d, k), k = 0..3  (uniform in +-1/sqrt(width))
+  conv bias    ~ U[-1/2, 1/2] per channel
+  history      ~ N(0, 1) per (b, d, 3), the inputs before the sequence
 Draw order: x, delta_raw, dt, A, B, C, D, z, h_init, from numpy's PCG64 seeded
 with the workload's seed.  bf16 inputs are the fp32 draws rounded to nearest
 even bfloat16 and are carried as raw uint16 bit patterns; A, D, delta_bias and
@@ -164,6 +168,23 @@ CONFIGS = {
     "long_bf16_16k": dict(batch=1, seqlen=16384, dim=2560, dstate=16, io="bf16", seed=4,
                           a_init="random", gate=True),
 }
+
+
+@dataclass
+class ConvPrologue:
+    w: np.ndarray                # (dim, 4) fp32, tap k multiplies the input k steps back
+    b: Optional[np.ndarray]      # (dim,) fp32
+    hist: Optional[np.ndarray]   # (batch, dim, 3) fp32, oldest first
+
+
+def make_conv(w: Workload, *, with_bias: bool = True, hist: bool = False, width: int = 4) -> ConvPrologue:
+    """Draw the block prologue's taps, bias and input history for a workload."""
+    rng = np.random.Generator(np.random.PCG64(w.seed + 7919))
+    bound = 1.0 / np.sqrt(width)
+    taps = rng.uniform(-bound, bound, size=(w.dim, width)).astype(np.float32)
+    bias = rng.uniform(-bound, bound, size=w.dim).astype(np.float32)
+    h = rng.standard_normal((w.batch, w.dim, width - 1), dtype=np.float32)
+    return ConvPrologue(taps, bias if with_bias else None, h if hist else None)
 
 
 def config(name: str) -> Workload:

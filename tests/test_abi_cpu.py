@@ -95,6 +95,32 @@ def test_exact_zoh_accepted_on_the_host():
     assert call(dims(bbar_mode=1)) == -5
 
 
+CP = {k: BASE + (12 + i) * (1 << 30) for i, k in enumerate(["cw", "cb", "cs"])}
+
+
+def call_conv(d, **over):
+    q = dict(P)
+    q.update(CP)
+    q.update(over)
+    return _abi.call_conv_fwd(q["x"], q["cw"], q["cb"], q["cs"], q["delta"], q["A"], q["B"], q["C"],
+                              q["D"], q["z"], q["bias"], q["out"], q["fs"], d, 0)
+
+
+def test_conv_entry_host_checks():
+    """The block-prologue entry checks its own arguments on the host: taps are
+    required, every pointer 16-byte aligned, the history disjoint from the other
+    tensors; the forms it is not built for (constant B and C, the exact-ZOH term,
+    N > 16) are SSM_ERR_UNSUPPORTED before anything touches the device."""
+    assert call_conv(dims(), cw=0) == -1
+    for k in ("cw", "cb", "cs"):
+        assert call_conv(dims(), **{k: CP[k] + 4}) == -3, k
+    assert call_conv(dims(), cs=P["out"]) == -6
+    assert call_conv(dims(), cs=P["fs"]) == -6
+    assert call_conv(dims(bc_layout=1)) == -4
+    assert call_conv(dims(bbar_mode=1)) == -4
+    assert call_conv(dims(dstate=32)) == -4
+
+
 def test_no_cpu_fallback():
     """A valid call without a usable GPU must fail, never compute on the host."""
     import torch
