@@ -175,30 +175,47 @@ def device_tensors(w, torch, device):
     return {k: dev(getattr(w, k)) for k in ("x", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0")}
 
 
-def oracle_sample(w, k):
+def oracle_sample(w, k, cv=None):
     """The float64 oracle, as it stands, on channels 0..k-1 of batch row 0 over the
-    full sequence length; returns seconds."""
+    full sequence length (with the block prologue when ``cv`` is given); returns
+    seconds."""
     import oracle
+    # the sample's inputs: batch row 0, channels 0..k-1 (sliced outside the timed region)
+    sl = lambda a: None if a is None else np.ascontiguousarray(a[:1, :, :k])
+    ch = lambda a: None if a is None else np.ascontiguousarray(a[:k])
+    x, delta, z = sl(w.x), sl(w.delta), sl(w.z)
+    A, D, bias = ch(w.A), ch(w.D), ch(w.delta_bias)
+    if w.per_channel_bc:
+        B, C = ch(w.B), ch(w.C)
+    else:
+        B, C = np.ascontiguousarray(w.B[:1]), np.ascontiguousarray(w.C[:1])
+    h0 = None if w.h0 is None else np.ascontiguousarray(w.h0[:1, :k])
     t = time.perf_counter()
-    oracle.selective_scan_channels([(0, d) for d in range(k)], w.x, w.delta, w.A, w.B, w.C,
-                                   D=w.D, z=w.z, delta_bias=w.delta_bias, h0=w.h0,
-                                   delta_softplus=w.delta_softplus, io_dtype=w.io)
+    if cv is None:
+        oracle.selective_scan(x, delta, A, B, C, D=D, z=z, delta_bias=bias, h0=h0,
+                              delta_softplus=w.delta_softplus, per_channel_bc=w.per_channel_bc,
+                              io_dtype=w.io)
+    else:
+        oracle.conv_selective_scan(x, ch(cv.w), ch(cv.b), None, delta, A, B, C, D=D, z=z,
+                                   delta_bias=bias, h0=h0, delta_softplus=w.delta_softplus,
+                                   io_dtype=w.io)
     return time.perf_counter() - t
 
 
-def cpu_baseline(w, budget_s: float = 15.0):
+def cpu_baseline(w, budget_s: float = 15.0, cv=None):
     import oracle
     cores = oracle.max_threads()
     cap = min(w.dim, 512)
     k = min(cap, max(cores, 8))
-    t = oracle_sample(w, k)
+    t = oracle_sample(w, k, cv)
     k2 = int(min(cap, max(k, k * budget_s / max(t, 1e-3))))
     k2 = max(1, (k2 // cores) * cores) if k2 >= cores else k2
     if k2 > k:
-        t, k = oracle_sample(w, k2), k2
+        t, k = oracle_sample(w, k2, cv), k2
     units = k * w.seqlen
+    what = "block prologue + scan" if cv is not None else "scan"
     return {"value": units / t, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, N={w.dstate} "
+            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, N={w.dstate}, {what} "
                       f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
 
 
@@ -225,6 +242,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--conv", action="store_true",
+                    help="the Mamba-block prologue (causal conv of width 4 + silu) fused in")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -260,11 +279,26 @@ def main():
 
     if state_in:
         fs.copy_(fs0)  # recurrent-step workload: each step advances the stored state
+    cv = cw = cb = cs = None
+    if args.conv:
+        from selective_state_space_112_b300.workloads import make_conv
+        cv = make_conv(w, hist=state_in)
+        cw = torch.from_numpy(cv.w).to(device)
+        cb = torch.from_numpy(cv.b).to(device)
+        cs = torch.from_numpy(cv.hist).to(device) if state_in else None
+
+    def scan(x, delta, A, B, C, D, z, bias, final_state):
+        if args.conv:
+            ssm.ssm_conv_selective_scan_fwd(x, cw, cb, cs, delta, A, B, C, D, z, bias, out=out,
+                                            final_state=final_state,
+                                            delta_softplus=w.delta_softplus, state_in=state_in)
+        else:
+            ssm.ssm_selective_scan_fwd(x, delta, A, B, C, D, z, bias, out=out,
+                                       final_state=final_state,
+                                       delta_softplus=w.delta_softplus, state_in=state_in)
 
     def step():
-        ssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
-                                   t["delta_bias"], out=out, final_state=fs,
-                                   delta_softplus=w.delta_softplus, state_in=state_in)
+        scan(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], fs)
 
     for _ in range(args.warmup):
         step()
@@ -307,7 +341,7 @@ def main():
     upd_peak = UPDATES_PER_SM_CLK * sms * sm_max * 1e6 / 1e9           # Gupdate/s
     upd_achieved = w.element_updates / (dom_ms * 1e-3) / 1e9
     tr = TRAFFIC.get(args.workload)
-    traffic = (tr["bytes_per_launch"] if tr and dom == "ssm_scan_output"
+    traffic = (tr["bytes_per_launch"] if tr and dom == "ssm_scan_output" and not args.conv
                and tr["kernel_src_sha"] == kernel_src_sha() else None)
     roof = {"bound": "alu", "kernel": dom, "achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
             "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
@@ -328,6 +362,7 @@ def main():
            "config": {"workload": args.workload, "batch": w.batch, "seqlen": w.seqlen,
                       "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io,
                       "gate": w.z is not None, "state_in": state_in,
+                      "prologue": "causal conv width 4 + silu" if args.conv else "none",
                       "parallelism": f"replica x{world}" if world > 1 else "single",
                       "l2": f"inputs {alg / 1e9:.2f} GB > 126 MB L2; no flush needed"
                             if alg > 4 * 126e6 else "L2 resident (latency case)"},
@@ -340,18 +375,23 @@ def main():
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
         dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        if args.conv:  # the prologue's taps and bias are inputs of every step too
+            conv_h = [(v, v.cpu().pin_memory()) for v in (cw, cb)]
+            host_extra = sum(h.numel() * h.element_size() for _, h in conv_h)
+        else:
+            conv_h, host_extra = [], 0
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None) + host_extra
         d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
 
         def e2e_step():
             for k, v in host.items():
                 if v is not None:
                     dev_in[k].copy_(v, non_blocking=True)
+            for d_t, h_t in conv_h:
+                d_t.copy_(h_t, non_blocking=True)
             fsd = dev_in["h0"] if state_in else fs
-            ssm.ssm_selective_scan_fwd(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"],
-                                       dev_in["C"], dev_in["D"], dev_in["z"], dev_in["delta_bias"],
-                                       out=out, final_state=fsd,
-                                       delta_softplus=w.delta_softplus, state_in=state_in)
+            scan(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
+                 dev_in["z"], dev_in["delta_bias"], fsd)
             out_h.copy_(out, non_blocking=True)
             fs_h.copy_(fsd, non_blocking=True)
 
@@ -373,7 +413,7 @@ def main():
                       "ms_per_step": ems / args.e2e_steps}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w)
+        res["cpu_baseline"] = cpu_baseline(w, cv=cv)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
