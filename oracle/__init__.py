@@ -71,6 +71,8 @@ def _load():
             lib.oracle_causal_conv.argtypes = [pd] * 4 + [i64] * 3 + [i32]
             lib.oracle_conv_silu.restype = i32
             lib.oracle_conv_silu.argtypes = [pd] * 6 + [i64] * 4 + [i32]
+            lib.oracle_selective_scan_bwd_f64.restype = i32
+            lib.oracle_selective_scan_bwd_f64.argtypes = [pd] * 20 + [i64] * 4 + [i32] * 2
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -210,6 +212,39 @@ def lti_kernel(A, B, C, dt, L: int, bbar_mode: int = 0):
     if rc != 0:
         raise ValueError("oracle_lti_kernel rejected its arguments")
     return K
+
+
+def selective_scan_bwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *,
+                       dout, dfinal=None, delta_softplus: bool = True, io_dtype: str = "f32",
+                       threads: int = 0):
+    """Gradients of ``selective_scan`` (bbar_mode 0, time-varying B and C) in float64.
+
+    ``dout``: (batch, L, dim) gradient of out; ``dfinal``: (batch, dim, N) gradient
+    of the final state or None.  Stored inputs are widened as in ``selective_scan``
+    (``dout`` is float64 or fp32 values).  Returns a dict with dx, ddelta, dA, dB,
+    dC, dD, dz (None without a gate), dbias and dh0, all float64.
+    """
+    x64, dl64, z64 = widen(x, io_dtype), widen(delta, io_dtype), widen(z, io_dtype)
+    B64, C64 = widen(B, io_dtype), widen(C, io_dtype)
+    A64, D64, bias64, h64 = widen(A), widen(D), widen(delta_bias), widen(h0)
+    g64, gf64 = widen(dout), widen(dfinal)
+    batch, L, dim = x64.shape
+    N = A64.shape[1]
+    assert B64.shape == (batch, L, N) and C64.shape == (batch, L, N) and g64.shape == x64.shape
+    r = {k: np.zeros(s_, dtype=np.float64) for k, s_ in (
+        ("dx", x64.shape), ("ddelta", x64.shape), ("dA", (dim, N)), ("dB", (batch, L, N)),
+        ("dC", (batch, L, N)), ("dD", (dim,)), ("dz", x64.shape), ("dbias", (dim,)),
+        ("dh0", (batch, dim, N)))}
+    rc = _load().oracle_selective_scan_bwd_f64(
+        _ptr(x64), _ptr(dl64), _ptr(A64), _ptr(B64), _ptr(C64), _ptr(D64), _ptr(z64), _ptr(bias64),
+        _ptr(h64), _ptr(g64), _ptr(gf64), _ptr(r["dx"]), _ptr(r["ddelta"]), _ptr(r["dA"]),
+        _ptr(r["dB"]), _ptr(r["dC"]), _ptr(r["dD"]), _ptr(r["dz"]), _ptr(r["dbias"]), _ptr(r["dh0"]),
+        batch, L, dim, N, int(delta_softplus), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_selective_scan_bwd_f64 rejected its arguments")
+    if z64 is None:
+        r["dz"] = None
+    return r
 
 
 CONV_WIDTH = 4  # taps of the Mamba block's depthwise causal convolution

@@ -33,6 +33,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -275,6 +276,127 @@ int oracle_conv_silu(const double* x, const double* w, const double* cb,
       for (int64_t j = 0; j < H; ++j)
         hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j);
 #undef XS
+  }
+  return 0;
+}
+
+/*
+ * Gradients of the selective-scan forward (bbar_mode 0, time-varying B and C),
+ * the backward pass with the states rebuilt rather than stored ("State-space
+ * models", section "The parallel scan": Mamba's kernel recomputes the expanded
+ * state in the backward pass).  Reverse-mode differentiation of the recurrence as
+ * oracle_selective_scan_f64 states it.  Per batch row b and channel d:
+ *
+ *   forward:  dt_t = softplus(v_t) (or v_t), v_t = delta_t + bias;
+ *             a_t[n] = exp(dt_t A[n]);  h_t = a_t h_{t-1} + dt_t B_t x_t;
+ *             y_t = C_t . h_t + D x_t;  out_t = y_t silu(z_t)
+ *   reverse:  gy_t = dout_t silu(z_t)  (dout_t without a gate)
+ *             lam_t = C_t gy_t + a_{t+1} lam_{t+1},  lam_{L-1} = C gy + dfinal
+ *             dA[n]   += lam_t[n] h_{t-1}[n] a_t[n] dt_t
+ *             ddt_t    = sum_n lam_t[n] (h_{t-1}[n] a_t[n] A[n] + B_t[n] x_t)
+ *             dx_t     = sum_n lam_t[n] dt_t B_t[n] + gy_t D
+ *             dB_t[n] += lam_t[n] dt_t x_t          (summed over channels)
+ *             dC_t[n] += gy_t h_t[n]                (summed over channels)
+ *             dz_t     = dout_t y_t silu'(z_t),  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *             ddelta_t = ddt_t sigmoid(v_t) (softplus) or ddt_t;  dbias += ddelta_t
+ *             dD      += gy_t x_t;   dh0 = a_0 lam_0
+ *
+ * h0 (batch, dim, N) may be NULL (zeros); dfinal (batch, dim, N) may be NULL
+ * (zeros); z, D, delta_bias may be NULL.  Outputs dx, ddelta, dz (when z),
+ * (batch, L, dim); dA (dim, N); dB, dC (batch, L, N); dD, dbias (dim); dh0
+ * (batch, dim, N) -- dz, dD, dbias, dh0 may be NULL.  The shared gradients
+ * (dA, dB, dC, dD, dbias) are zeroed here and summed over channels.
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_selective_scan_bwd_f64(
+    const double* x, const double* delta, const double* A, const double* B,
+    const double* C, const double* D, const double* z, const double* delta_bias,
+    const double* h0, const double* dout, const double* dfinal, double* dx,
+    double* ddelta, double* dA, double* dB, double* dC, double* dD, double* dz,
+    double* dbias, double* dh0, int64_t batch, int64_t seqlen, int64_t dim,
+    int64_t dstate, int delta_softplus, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || dstate > 64) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const int64_t N = dstate, L = seqlen;
+  for (int64_t i = 0; i < dim * N; ++i) dA[i] = 0.0;
+  for (int64_t i = 0; i < batch * L * N; ++i) dB[i] = dC[i] = 0.0;
+  for (int64_t d = 0; d < dim; ++d) {
+    if (dD) dD[d] = 0.0;
+    if (dbias) dbias[d] = 0.0;
+  }
+  const int64_t nchan = batch * dim;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ch = 0; ch < nchan; ++ch) {
+    const int64_t b = ch / dim;
+    const int64_t d = ch % dim;
+    /* forward, keeping every state: hs[(t + 1) N + n] = h_t[n], hs[n] = h_{-1}[n] */
+    double* hs = (double*)malloc(sizeof(double) * (size_t)(L + 1) * N);
+    double* dts = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double* vs = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[(b * dim + d) * N + n] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t i = (b * L + t) * dim + d;
+      vs[t] = delta[i] + (delta_bias ? delta_bias[d] : 0.0);
+      dts[t] = delta_softplus ? oracle_softplus(vs[t]) : vs[t];
+      for (int64_t n = 0; n < N; ++n)
+        hs[(t + 1) * N + n] = exp(dts[t] * A[d * N + n]) * hs[t * N + n] +
+                              dts[t] * B[(b * L + t) * N + n] * x[i];
+    }
+    /* reverse */
+    double lam_next[64], a_next[64];
+    for (int64_t n = 0; n < N; ++n) {
+      lam_next[n] = dfinal ? dfinal[(b * dim + d) * N + n] : 0.0;
+      a_next[n] = 1.0; /* the final-state gradient enters lam_{L-1} undecayed */
+    }
+    double sD = 0.0, sbias = 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+      const int64_t i = (b * L + t) * dim + d;
+      const double* Bt = &B[(b * L + t) * N];
+      const double* Ct = &C[(b * L + t) * N];
+      const double sz = z ? 1.0 / (1.0 + exp(-z[i])) : 1.0;
+      const double gy = z ? dout[i] * z[i] * sz : dout[i];
+      double ddt = 0.0, gx = 0.0, y = 0.0;
+      for (int64_t n = 0; n < N; ++n) {
+        const double a = exp(dts[t] * A[d * N + n]);
+        const double lam = Ct[n] * gy + a_next[n] * lam_next[n];
+        const double hprev = hs[t * N + n], hcur = hs[(t + 1) * N + n];
+#pragma omp atomic
+        dA[d * N + n] += lam * hprev * a * dts[t];
+        ddt += lam * (hprev * a * A[d * N + n] + Bt[n] * x[i]);
+        gx += lam * dts[t] * Bt[n];
+#pragma omp atomic
+        dB[(b * L + t) * N + n] += lam * dts[t] * x[i];
+#pragma omp atomic
+        dC[(b * L + t) * N + n] += gy * hcur;
+        y += Ct[n] * hcur;
+        lam_next[n] = lam;
+        a_next[n] = a;
+      }
+      y += (D ? D[d] : 0.0) * x[i];
+      dx[i] = gx + gy * (D ? D[d] : 0.0);
+      if (z && dz) dz[i] = dout[i] * y * sz * (1.0 + z[i] * (1.0 - sz));
+      const double sv = delta_softplus ? 1.0 / (1.0 + exp(-vs[t])) : 1.0;
+      ddelta[i] = ddt * sv;
+      sbias += ddt * sv;
+      sD += gy * x[i];
+    }
+    if (dh0)
+      for (int64_t n = 0; n < N; ++n) dh0[(b * dim + d) * N + n] = a_next[n] * lam_next[n];
+    if (dD) {
+#pragma omp atomic
+      dD[d] += sD;
+    }
+    if (dbias) {
+#pragma omp atomic
+      dbias[d] += sbias;
+    }
+    free(hs);
+    free(dts);
+    free(vs);
   }
   return 0;
 }

@@ -40,6 +40,16 @@ MUTANTS = {
     "conv_no_silu": ("u[(b * seqlen + t) * dim + d] = silu(pre);", "u[(b * seqlen + t) * dim + d] = pre;"),
     "conv_hist_out_shift": ("hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j);",
                             "hist_out[(b * dim + d) * H + j] = XS(seqlen - H + j - 1);"),
+    "bwd_lambda_uses_own_decay": ("const double lam = Ct[n] * gy + a_next[n] * lam_next[n];",
+                                  "const double lam = Ct[n] * gy + a * lam_next[n];"),
+    "bwd_dC_previous_state": ("dC[(b * L + t) * N + n] += gy * hcur;", "dC[(b * L + t) * N + n] += gy * hprev;"),
+    "bwd_ddelta_no_sigmoid": ("const double sv = delta_softplus ? 1.0 / (1.0 + exp(-vs[t])) : 1.0;",
+                              "const double sv = 1.0;"),
+    "bwd_dx_no_skip": ("dx[i] = gx + gy * (D ? D[d] : 0.0);", "dx[i] = gx;"),
+    "bwd_dA_no_step": ("dA[d * N + n] += lam * hprev * a * dts[t];", "dA[d * N + n] += lam * hprev * a;"),
+    "bwd_dz_plain_sigmoid": ("dz[i] = dout[i] * y * sz * (1.0 + z[i] * (1.0 - sz));", "dz[i] = dout[i] * y * sz;"),
+    "bwd_dh0_undecayed": ("dh0[(b * dim + d) * N + n] = a_next[n] * lam_next[n];",
+                          "dh0[(b * dim + d) * N + n] = lam_next[n];"),
 }
 
 

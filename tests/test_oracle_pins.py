@@ -460,3 +460,89 @@ def test_conv_scan_composes_prologue_and_scan():
     np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-14)
     np.testing.assert_allclose(st, ref_st, rtol=1e-14, atol=1e-14)
     np.testing.assert_array_equal(hout, w.x[:, -3:, :].transpose(0, 2, 1).astype(np.float64))
+
+
+# ------------------------------------------------------------------ backward pass
+# "State-space models", section "The parallel scan": the fused kernel rebuilds the
+# expanded state in the backward pass.  The oracle's gradients are pinned against
+# central finite differences of the forward oracle, and against torch autograd
+# through a separately written float64 forward.
+
+def _bwd_case(seed, *, gate=True, with_D=True, with_bias=True, state_in=True, softplus=True):
+    w = make_workload("bwd", batch=2, seqlen=7, dim=3, dstate=4, io="f32", seed=seed, gate=gate,
+                      with_D=with_D, with_bias=with_bias, state_in=state_in)
+    rng = np.random.default_rng(seed + 100)
+    f = lambda a: None if a is None else np.asarray(a, dtype=np.float64).copy()
+    inp = dict(x=f(w.x), delta=f(w.delta), A=f(w.A), B=f(w.B), C=f(w.C), D=f(w.D), z=f(w.z),
+               delta_bias=f(w.delta_bias), h0=f(w.h0))
+    if not softplus:  # raw steps, small and positive
+        inp["delta"] = np.abs(inp["delta"]) * 0.3
+        inp["delta_bias"] = None
+    dout = rng.standard_normal(w.x.shape)
+    dfinal = rng.standard_normal((w.batch, w.dim, w.dstate)) if state_in else None
+    return inp, dout, dfinal, softplus
+
+
+def _loss(inp, dout, dfinal, softplus):
+    out, st = oracle.selective_scan(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                    inp["z"], inp["delta_bias"], inp["h0"], delta_softplus=softplus)
+    return float(np.sum(out * dout) + (np.sum(st * dfinal) if dfinal is not None else 0.0))
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(gate=False, with_D=False),
+                                     dict(with_bias=False, state_in=False), dict(softplus=False)],
+                         ids=["full", "no_gate_no_D", "no_bias_no_state", "no_softplus"])
+def test_backward_matches_finite_differences(variant):
+    """Every gradient the oracle returns equals the central difference of the loss
+    sum(dout * out) + sum(dfinal * final_state) under the forward oracle."""
+    inp, dout, dfinal, sp = _bwd_case(3, **variant)
+    g = oracle.selective_scan_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["delta_bias"], inp["h0"], dout=dout, dfinal=dfinal,
+                                  delta_softplus=sp)
+    names = [("x", "dx"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("D", "dD"),
+             ("z", "dz"), ("delta_bias", "dbias"), ("h0", "dh0")]
+    for arg, gname in names:
+        if inp[arg] is None:
+            continue
+        base = inp[arg]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            eps = 1e-6 * max(1.0, abs(base[idx]))
+            old = base[idx]
+            base[idx] = old + eps
+            lp = _loss(inp, dout, dfinal, sp)
+            base[idx] = old - eps
+            lm = _loss(inp, dout, dfinal, sp)
+            base[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gname], fd, rtol=2e-6, atol=2e-7, err_msg=gname)
+
+
+def test_backward_matches_autograd_of_an_independent_forward():
+    """torch autograd through a float64 forward written with cumulative sums of the
+    step sizes (exp(A (S_t - S_s)) weights) instead of the recurrence."""
+    torch = pytest.importorskip("torch")
+    inp, dout, dfinal, sp = _bwd_case(5)
+    T = {k: (None if v is None else torch.tensor(v, dtype=torch.float64, requires_grad=True))
+         for k, v in inp.items()}
+    v = T["delta"] + T["delta_bias"]
+    dt = torch.nn.functional.softplus(v)                                  # (b, L, d)
+    S = torch.cumsum(dt, dim=1)                                           # S_t = sum_{s<=t} dt_s
+    # h_t[n] = exp(A (S_t)) h0 + sum_{s<=t} exp(A (S_t - S_s)) dt_s B_s x_s
+    Ab = T["A"][None, None]                                               # (1, 1, d, n)
+    decay_all = torch.exp(Ab * S[..., None])                              # (b, L, d, n)
+    L = dt.shape[1]
+    mask = torch.tril(torch.ones(L, L, dtype=torch.float64))              # s <= t
+    W = torch.exp(Ab[:, :, None] * (S[:, :, None, :, None] - S[:, None, :, :, None]))  # (b, t, s, d, n)
+    W = W * mask[None, :, :, None, None]
+    inj = dt[..., None] * T["B"][:, :, None, :] * T["x"][..., None]       # (b, s, d, n)
+    h = decay_all * T["h0"][:, None] + torch.einsum("btsdn,bsdn->btdn", W, inj)
+    y = torch.einsum("btdn,btn->btd", h, T["C"]) + T["D"] * T["x"]
+    out = y * T["z"] * torch.sigmoid(T["z"])
+    loss = (out * torch.tensor(dout)).sum() + (h[:, -1] * torch.tensor(dfinal)).sum()
+    loss.backward()
+    g = oracle.selective_scan_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["delta_bias"], inp["h0"], dout=dout, dfinal=dfinal)
+    for arg, gname in [("x", "dx"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"),
+                       ("D", "dD"), ("z", "dz"), ("delta_bias", "dbias"), ("h0", "dh0")]:
+        np.testing.assert_allclose(g[gname], T[arg].grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=gname)
