@@ -20,7 +20,8 @@ MUTANTS = {
     "skip_dropped": ("y += (D ? D[d] : 0.0) * xv;", "y += 0.0 * xv;"),
     "gate_no_sigmoid": ("if (z) y *= silu(z[i]);", "if (z) y *= z[i];"),
     "softplus_sign": ("log1p(exp(-fabs(v)))", "log1p(exp(fabs(v)))"),
-    "bias_sign": ("delta[i] + (delta_bias ? delta_bias[d] : 0.0)", "delta[i] - (delta_bias ? delta_bias[d] : 0.0)"),
+    "bias_sign": ("const double v = delta[i] + (delta_bias ? delta_bias[d] : 0.0);",
+                  "const double v = delta[i] - (delta_bias ? delta_bias[d] : 0.0);"),
     "B_time_shift": (": &B[(b * seqlen + t) * dstate];", ": &B[(b * seqlen + (t > 0 ? t - 1 : 0)) * dstate];"),
     "state_in_ignored": ("h[n] = state_in ? state[(b * dim + d) * dstate + n] : 0.0;", "h[n] = 0.0;"),
     "zoh_missing_div_a": ("bbar = (a != 0.0) ? expm1(dt * a) / a * Bv[n] : dt * Bv[n];",
