@@ -1,5 +1,6 @@
 /*
- * ssm_scan.h -- C ABI of the B300 (sm_103a) Mamba S6 selective-scan forward.
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) Mamba S6 selective scan (forward,
+ * the forward with the Mamba-block prologue, and the backward pass).
  *
  * The operation (pages "State-space models", rayaq.ca, sections
  * "Discretization", "Mamba: selection", "The parallel scan" and
@@ -139,6 +140,46 @@ int ssm_conv_selective_scan_fwd(const void* x, const float* conv_w, const float*
                                 const void* z, const float* delta_bias, void* out,
                                 float* final_state, const ssm_dims* dims,
                                 cudaStream_t stream);
+
+/*
+ * Selective-scan backward: the gradients of ssm_selective_scan_fwd (bbar_mode 0,
+ * time-varying B and C, dstate <= 16) with the expanded state rebuilt rather than
+ * stored (page "State-space models", section "The parallel scan": Mamba's kernel
+ * recomputes the state in the backward pass).  With gy_t = dout_t * silu(z_t) and
+ * the adjoint state lam_t = C_t gy_t + Abar_{t+1} lam_{t+1} (lam_{L-1} = C gy +
+ * dfinal_state), for every b, t, d, n:
+ *
+ *   dx      = sum_n lam step B + gy D          ddelta = d(step)/d(delta) * (
+ *   dA[d,n] = sum_{b,t} lam h_{t-1} Abar step       sum_n lam (h_{t-1} Abar A + B x) )
+ *   dB[b,t,n] = sum_d lam step x               dC[b,t,n] = sum_d gy h_t
+ *   dD[d]   = sum_{b,t} gy x                   ddelta_bias[d] = sum_{b,t} ddelta
+ *   dz      = dout y silu'(z)                  dh_init = Abar_0 lam_0
+ *
+ *   x, delta, A, B, C, D, z, delta_bias : as ssm_selective_scan_fwd (dims likewise;
+ *                  dims->state_in is not used: h_init says whether there is one)
+ *   h_init       : (batch, dim, dstate) fp32 initial state, or NULL (zeros)
+ *   dout         : (batch, seqlen, dim) io dtype, gradient of out
+ *   dfinal_state : (batch, dim, dstate) fp32 gradient of the final state, or NULL
+ *   dx, ddelta   : (batch, seqlen, dim) io dtype, written
+ *   dz           : (batch, seqlen, dim) io dtype, written; required when z is given
+ *   dA           : (dim, dstate) fp32; dB, dC: (batch, seqlen, dstate) fp32;
+ *   dD, ddelta_bias : (dim) fp32 or NULL -- these sums are overwritten (zeroed first)
+ *   dh_init      : (batch, dim, dstate) fp32 or NULL
+ * No output may overlap an input or another output.  Sums over channels are
+ * accumulated with fp32 atomic additions, so their rounding order is not fixed.
+ * Other forms return SSM_ERR_UNSUPPORTED.  Long sequences are chunked; the
+ * workspace (chunk carries and a state checkpoint every 16 steps:
+ * ceil(seqlen / 16) * batch * dim * padded dstate fp32) comes from the library's
+ * stream-ordered pool.
+ */
+int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A,
+                           const void* B, const void* C, const float* D,
+                           const void* z, const float* delta_bias,
+                           const float* h_init, const void* dout,
+                           const float* dfinal_state, void* dx, void* ddelta,
+                           float* dA, float* dB, float* dC, float* dD, void* dz,
+                           float* ddelta_bias, float* dh_init, const ssm_dims* dims,
+                           cudaStream_t stream);
 
 /* Bytes of the fixed workspace of ssm_selective_scan_fwd_noalloc (16 MiB). */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)

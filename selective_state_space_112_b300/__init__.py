@@ -11,7 +11,8 @@ from . import _abi
 from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, SSM_OK,
                    SSMError, SsmDims)
 
-__all__ = ["ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc",
+__all__ = ["ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_bwd",
+           "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read", "SSMError", "SsmDims"]
@@ -73,6 +74,63 @@ def ssm_conv_selective_scan_fwd(x, conv_w, conv_b, conv_state, delta, A, B, C, D
     return _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state,
                  (conv_w, conv_b, conv_state), delta_softplus=delta_softplus, state_in=state_in,
                  bbar_mode=0, return_final_state=return_final_state, stream=stream, noalloc=False)
+
+
+def ssm_selective_scan_bwd(x, delta, A, B, C, D, z, delta_bias, h_init, dout, dfinal_state=None,
+                           *, delta_softplus: bool = True, stream=None):
+    """Gradients of ``ssm_selective_scan_fwd`` (time-varying B, C; bbar_mode 0).
+
+    Inputs as the forward (h_init: (batch, dim, N) float32 or None); dout: gradient of
+    out, same shape and dtype as x; dfinal_state: gradient of the final state (float32)
+    or None.  Returns a dict: dx, ddelta, dz (io dtype; dz None without a gate),
+    dA (dim, N), dB, dC (batch, L, N), dD, ddelta_bias (dim,), dh_init (batch, dim, N)
+    -- all float32 except dx, ddelta, dz; dD / ddelta_bias / dh_init are None when D /
+    delta_bias / h_init are.
+    """
+    torch = _torch()
+    if x.dtype == torch.float32:
+        io = SSM_F32
+    elif x.dtype == torch.bfloat16:
+        io = SSM_BF16
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    batch, L, dim = x.shape
+    N = A.shape[-1]
+    if B.dim() != 3:
+        raise ValueError("the backward pass takes time-varying B and C (batch, L, N)")
+    for name, t, dt, shp in (
+            ("delta", delta, x.dtype, x.shape), ("z", z, x.dtype, x.shape), ("dout", dout, x.dtype, x.shape),
+            ("A", A, torch.float32, (dim, N)), ("D", D, torch.float32, (dim,)),
+            ("delta_bias", delta_bias, torch.float32, (dim,)), ("B", B, x.dtype, (batch, L, N)),
+            ("C", C, x.dtype, (batch, L, N)), ("h_init", h_init, torch.float32, (batch, dim, N)),
+            ("dfinal_state", dfinal_state, torch.float32, (batch, dim, N))):
+        if t is None:
+            continue
+        if t.dtype != dt or tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{name}: expected {dt} {tuple(shp)}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+         "dz": torch.empty_like(x) if z is not None else None,
+         "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, L, N), **f32),
+         "dC": torch.empty((batch, L, N), **f32),
+         "dD": torch.empty((dim,), **f32) if D is not None else None,
+         "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+         "dh_init": torch.empty((batch, dim, N), **f32) if h_init is not None else None}
+    dims = SsmDims(batch=batch, seqlen=L, dim=dim, dstate=N, io_dtype=io, bc_layout=SSM_BC_TIME_VARYING,
+                   delta_softplus=int(bool(delta_softplus)), state_in=0, bbar_mode=0, reserved=0)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    addrs = [_addr(t) for t in (x, delta, A, B, C, D, z, delta_bias, h_init, dout, dfinal_state,
+                                g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"],
+                                g["ddelta_bias"], g["dh_init"])]
+    rc = _abi.call_bwd(addrs, dims, int(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_selective_scan_bwd")
+    return g
 
 
 def _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state, conv, *, delta_softplus,

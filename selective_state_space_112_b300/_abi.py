@@ -25,7 +25,8 @@ SSM_OK = 0
 SSM_ERR_SCRATCH = -10
 SSM_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/ssm_scan.h
 # names as declared in include/ssm_scan.h
-EXPORTS = ("ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_fwd_noalloc",
+EXPORTS = ("ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_bwd",
+           "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read")
@@ -67,6 +68,8 @@ def lib():
             L.ssm_selective_scan_fwd.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_conv_selective_scan_fwd.restype = i32
             L.ssm_conv_selective_scan_fwd.argtypes = [vp] * 13 + [ctypes.POINTER(SsmDims), vp]
+            L.ssm_selective_scan_bwd.restype = i32
+            L.ssm_selective_scan_bwd.argtypes = [vp] * 20 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_selective_scan_fwd_noalloc.restype = i32
             L.ssm_selective_scan_fwd_noalloc.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_check_status.restype = i32
@@ -110,6 +113,13 @@ def call_conv_fwd(x, conv_w, conv_b, conv_state, delta, A, B, C, D, z, delta_bia
         x or None, conv_w or None, conv_b or None, conv_state or None, delta or None, A or None,
         B or None, C or None, D or None, z or None, delta_bias or None, out or None,
         final_state or None, ctypes.byref(dims), stream or None)
+
+
+def call_bwd(addrs, dims: SsmDims, stream) -> int:
+    """Raw call of ssm_selective_scan_bwd: ``addrs`` holds the 20 tensor addresses in
+    declaration order (0 = NULL)."""
+    assert len(addrs) == 20
+    return lib().ssm_selective_scan_bwd(*[a or None for a in addrs], ctypes.byref(dims), stream or None)
 
 
 def check_status(stream=0) -> int:

@@ -1,0 +1,270 @@
+// Backward pass of the selective scan with the states rebuilt rather than stored
+// (page "State-space models", section "The parallel scan": Mamba's kernel recomputes
+// the expanded state in the backward pass).  Reverse-mode differentiation of
+//   dt_t = softplus(v_t), v_t = delta_t + bias;  a_t = exp(dt_t A);
+//   h_t = a_t h_{t-1} + dt_t B_t x_t;  y_t = C_t . h_t + D x_t;  out_t = y_t silu(z_t)
+// with the adjoint state lam_t = C_t gy_t + a_{t+1} lam_{t+1} (gy_t = dout_t silu(z_t)).
+//
+// Design: one warp per CTA, one lane per channel, all S (= padded N) states of the
+// channel in the lane.  The sequence is cut into chunks scanned in parallel; the
+// carries in both directions use the associative combine of the per-step maps:
+//  * forward: the aggregate pass of the forward kernel (chunk end state from a zero
+//    start, chunk step sum S_c) gives h at each chunk start, h <- exp(A S_c) h + H_c;
+//  * reverse: bwd_reverse_aggregate gives each chunk's adjoint carry from a zero
+//    start at its end, M_c = sum_s (prod_{r=t0..s} a_r) C_s gy_s, and its own S_c; the
+//    carry into chunk c from the right is mu_c = M_{c+1} + exp(A S_{c+1}) mu_{c+1},
+//    mu = dfinal past the last chunk.
+// bwd_main then sweeps its chunk forward once, storing h every SEG steps (HBM
+// checkpoints), and walks the segments backwards: it rebuilds the segment's states
+// into shared memory and runs the adjoint sweep over them.  dB, dC (summed over
+// channels) leave through a warp reduce-scatter and one atomic add per (t, n) per
+// warp; dA, dD and the bias gradient accumulate in registers and are added once per
+// lane.
+#include <cuda_runtime.h>
+
+#include "bwd_kernel.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int SEG = 16;  // steps per rebuilt segment (chunk lengths are multiples of 32)
+
+template <typename IO, int S>
+__device__ __forceinline__ void load_row_g(const void* base, int64_t row, int N, float (&v)[S]) {
+#pragma unroll
+  for (int n = 0; n < S; ++n) v[n] = n < N ? IO::load(base, row * N + n) : 0.f;
+}
+
+__device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
+
+// Lane i receives the warp sum of v[i] (32 values per lane): recursive halving.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+}  // namespace
+
+// Reverse chunk aggregates of chunks 1 .. nchunks-1 (grid.y = chunk - 1).
+template <typename IO, int S>
+__global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
+  const int lane = threadIdx.x;
+  const int64_t L = p.seqlen, Dm = p.dim;
+  const int N = p.dstate;
+  const int b = blockIdx.z, chunk = blockIdx.y + 1;
+  const int64_t d = (int64_t)blockIdx.x * 32 + lane;
+  const bool valid = d < Dm;
+  const int64_t dd = valid ? d : Dm - 1;
+  const int64_t t0 = (int64_t)chunk * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  float A2[S], m[S];
+#pragma unroll
+  for (int n = 0; n < S; ++n) {
+    A2[n] = n < N ? p.A[dd * N + n] * kLog2e : 0.f;
+    m[n] = 0.f;
+  }
+  const float biasv = p.bias ? p.bias[dd] : 0.f;
+  float Ssum = 0.f, Scomp = 0.f;
+  for (int64_t t = t1 - 1; t >= t0; --t) {
+    const int64_t i = ((int64_t)b * L + t) * Dm + dd;
+    const float v = IO::load(p.delta, i) + biasv;
+    const float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
+    const float g = IO::load(p.dout, i);
+    const float gy = p.z ? g * silu(IO::load(p.z, i)) : g;
+    float c[S];
+    load_row_g<IO, S>(p.C, (int64_t)b * L + t, N, c);
+#pragma unroll
+    for (int n = 0; n < S; ++n) m[n] = ex2(dt * A2[n]) * fmaf(c[n], gy, m[n]);
+    kahan_add(Ssum, Scomp, dt);
+  }
+  if (!valid) return;
+  const int64_t ci = ((int64_t)(chunk - 1) * p.batch + b) * Dm + d;
+#pragma unroll
+  for (int n = 0; n < S; ++n)
+    if (n < N) p.ws_M[ci * N + n] = m[n];
+  p.ws_S2[ci] = Ssum - Scomp;
+}
+
+template <typename IO, int S>
+__global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
+  __shared__ float hist[SEG + 1][S][32];  // row 0: state before the segment
+  __shared__ float dts[SEG][32], vs[SEG][32];
+  const int lane = threadIdx.x;
+  const int64_t L = p.seqlen, Dm = p.dim;
+  const int N = p.dstate;
+  const int b = blockIdx.z, chunk = blockIdx.y;
+  const int64_t d = (int64_t)blockIdx.x * 32 + lane;
+  const bool valid = d < Dm;
+  const int64_t dd = valid ? d : Dm - 1;
+  const int64_t t0 = (int64_t)chunk * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const bool sp = p.delta_softplus != 0;
+
+  float A2[S];
+#pragma unroll
+  for (int n = 0; n < S; ++n) A2[n] = n < N ? p.A[dd * N + n] * kLog2e : 0.f;
+  const float biasv = p.bias ? p.bias[dd] : 0.f;
+  const float Dv = p.Dskip ? p.Dskip[dd] : 0.f;
+  const int64_t sidx = ((int64_t)b * Dm + dd) * N;
+
+  // ---- state at the chunk start (forward carry)
+  float h[S];
+#pragma unroll
+  for (int n = 0; n < S; ++n) h[n] = (chunk == 0 && p.h_init && n < N) ? p.h_init[sidx + n] : 0.f;
+  for (int cc = 0; cc < chunk; ++cc) {
+    const int64_t ci = ((int64_t)cc * p.batch + b) * Dm + dd;
+    const float Sc = p.ws_S[ci];
+#pragma unroll
+    for (int n = 0; n < S; ++n)
+      if (n < N) h[n] = fmaf(ex2(Sc * A2[n]), h[n], p.ws_H[ci * N + n]);
+  }
+  // ---- adjoint carry into the chunk from the right: kap = a_{t1} lam_{t1}
+  float kap[S];
+#pragma unroll
+  for (int n = 0; n < S; ++n) kap[n] = (p.dfinal && n < N) ? p.dfinal[sidx + n] : 0.f;
+  for (int cc = p.nchunks - 1; cc > chunk; --cc) {
+    const int64_t ci = ((int64_t)(cc - 1) * p.batch + b) * Dm + dd;
+    const float Sc = p.ws_S2[ci];
+#pragma unroll
+    for (int n = 0; n < S; ++n)
+      if (n < N) kap[n] = fmaf(ex2(Sc * A2[n]), kap[n], p.ws_M[ci * N + n]);
+  }
+
+  // ---- forward sweep: checkpoints at every segment start
+  const int nseg = (int)((t1 - t0 + SEG - 1) / SEG);
+  const int64_t seg0 = t0 / SEG;
+  for (int64_t t = t0; t < t1; ++t) {
+    if ((t - t0) % SEG == 0 && valid) {
+      float* ck = p.ws_ck + (((seg0 + (t - t0) / SEG) * p.batch + b) * Dm + d) * S;
+#pragma unroll
+      for (int n = 0; n < S; ++n) ck[n] = h[n];
+    }
+    const int64_t i = ((int64_t)b * L + t) * Dm + dd;
+    const float v = IO::load(p.delta, i) + biasv;
+    const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
+    const float u = dt * IO::load(p.x, i);
+    float bv[S];
+    load_row_g<IO, S>(p.B, (int64_t)b * L + t, N, bv);
+#pragma unroll
+    for (int n = 0; n < S; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], u * bv[n]);
+  }
+
+  // ---- segments in reverse: rebuild the states, then the adjoint sweep
+  float gA[S];
+#pragma unroll
+  for (int n = 0; n < S; ++n) gA[n] = 0.f;
+  float gD = 0.f, gbias = 0.f;
+  for (int j = nseg - 1; j >= 0; --j) {
+    const int64_t ts = t0 + (int64_t)j * SEG, te = min(ts + SEG, t1);
+    const int cnt = (int)(te - ts);
+    __syncwarp();  // the previous segment's readers are done with the buffers
+    {
+      const float* ck = p.ws_ck + (((seg0 + j) * p.batch + b) * Dm + dd) * S;
+#pragma unroll
+      for (int n = 0; n < S; ++n) h[n] = valid ? ck[n] : 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < S; ++n) hist[0][n][lane] = h[n];
+    for (int k = 0; k < cnt; ++k) {
+      const int64_t i = ((int64_t)b * L + ts + k) * Dm + dd;
+      const float v = IO::load(p.delta, i) + biasv;
+      const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
+      dts[k][lane] = dt;
+      vs[k][lane] = v;
+      const float u = dt * IO::load(p.x, i);
+      float bv[S];
+      load_row_g<IO, S>(p.B, (int64_t)b * L + ts + k, N, bv);
+#pragma unroll
+      for (int n = 0; n < S; ++n) {
+        h[n] = fmaf(ex2(dt * A2[n]), h[n], u * bv[n]);
+        hist[k + 1][n][lane] = h[n];
+      }
+    }
+    for (int k = cnt - 1; k >= 0; --k) {
+      const int64_t t = ts + k;
+      const int64_t i = ((int64_t)b * L + t) * Dm + dd;
+      const float dt = dts[k][lane], v = vs[k][lane];
+      const float xv = IO::load(p.x, i), g = IO::load(p.dout, i);
+      float zv = 0.f, sz = 1.f;
+      if (p.z) {
+        zv = IO::load(p.z, i);
+        sz = sigmoidf_(zv);
+      }
+      const float gy = p.z ? g * zv * sz : g;
+      float bv[S], cv[S];
+      load_row_g<IO, S>(p.B, (int64_t)b * L + t, N, bv);
+      load_row_g<IO, S>(p.C, (int64_t)b * L + t, N, cv);
+      float ddt = 0.f, gx = 0.f, y = 0.f;
+      float red[32];
+#pragma unroll
+      for (int n = 0; n < S; ++n) {
+        const float a = ex2(dt * A2[n]);
+        const float hp = hist[k][n][lane], hc = hist[k + 1][n][lane];
+        const float lam = fmaf(cv[n], gy, kap[n]);
+        const float ga = lam * hp * a;  // gradient of a_t, times a_t
+        gA[n] = fmaf(ga, dt, gA[n]);
+        ddt = fmaf(ga, A2[n] * kLn2, fmaf(lam, bv[n] * xv, ddt));
+        gx = fmaf(lam, bv[n], gx);
+        y = fmaf(cv[n], hc, y);
+        red[n] = valid ? lam * dt * xv : 0.f;       // this channel's share of dB
+        red[16 + n] = valid ? gy * hc : 0.f;        // and of dC
+        kap[n] = a * lam;
+      }
+#pragma unroll
+      for (int n = S; n < 16; ++n) red[n] = red[16 + n] = 0.f;
+      gx = fmaf(gy, Dv, gx * dt);
+      y = fmaf(Dv, xv, y);
+      const float dv = sp ? ddt * sigmoidf_(v) : ddt;
+      gbias += dv;
+      gD = fmaf(gy, xv, gD);
+      if (valid) {
+        IO::store(p.dx, i, gx);
+        IO::store(p.ddelta, i, dv);
+        if (p.z) IO::store(p.dz, i, g * y * sz * fmaf(zv, 1.f - sz, 1.f));
+      }
+      const float tot = reduce_scatter32(red, lane);
+      const int n = lane & 15;
+      if (n < N) atomicAdd((lane < 16 ? p.dB : p.dC) + ((int64_t)b * L + t) * N + n, tot);
+    }
+  }
+  if (!valid) return;
+  // kap = a_{t0} lam_{t0}: the gradient of the state before the chunk
+  if (chunk == 0 && p.dh_init)
+#pragma unroll
+    for (int n = 0; n < S; ++n)
+      if (n < N) p.dh_init[sidx + n] = kap[n];
+#pragma unroll
+  for (int n = 0; n < S; ++n)
+    if (n < N) atomicAdd(p.dA + dd * N + n, gA[n]);
+  if (p.dD) atomicAdd(p.dD + dd, gD);
+  if (p.dbias) atomicAdd(p.dbias + dd, gbias);
+}
+
+template <typename IO, int S>
+BwdKernels bwd_kernels() {
+  BwdKernels k;
+  k.reverse_aggregate = bwd_reverse_aggregate<IO, S>;
+  k.main = bwd_main<IO, S>;
+  k.seg = SEG;
+  return k;
+}
+
+BwdKernels lookup_bwd(int io_bf16, int S) {
+  switch (S) {
+    case 2: return io_bf16 ? bwd_kernels<BF16, 2>() : bwd_kernels<F32, 2>();
+    case 4: return io_bf16 ? bwd_kernels<BF16, 4>() : bwd_kernels<F32, 4>();
+    case 8: return io_bf16 ? bwd_kernels<BF16, 8>() : bwd_kernels<F32, 8>();
+    case 16: return io_bf16 ? bwd_kernels<BF16, 16>() : bwd_kernels<F32, 16>();
+    default: return BwdKernels();
+  }
+}
+
+}  // namespace ssm

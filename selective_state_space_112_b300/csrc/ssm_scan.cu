@@ -15,6 +15,7 @@
 #include <utility>
 #include <vector>
 
+#include "bwd_kernel.h"
 #include "kernel_table.cuh"
 #include "scan_internal.h"
 
@@ -45,7 +46,9 @@ struct ProfRec {
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof;
-const char* const kKindName[3] = {"ssm_chunk_aggregate", "ssm_scan_output", "ssm_step"};
+constexpr int kKinds = 5;
+const char* const kKindName[kKinds] = {"ssm_chunk_aggregate", "ssm_scan_output", "ssm_step",
+                                      "ssm_bwd_reverse_aggregate", "ssm_bwd_main"};
 
 // ------------------------------------------------------- per-device pools
 
@@ -269,6 +272,30 @@ int launch(const ssm::KernelInfo& kn, int kind, dim3 grid, const ssm::TmaMaps& m
   return SSM_OK;
 }
 
+// Launch of a backward-pass kernel (one warp per CTA), with the same profiling hook.
+int launch_bwd(ssm::BwdFn fn, int kind, dim3 grid, const ssm::BwdParams& p, cudaStream_t stream) {
+  if (!fn) return SSM_ERR_CUDA;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaEventRecord(e0, stream) != cudaSuccess) return SSM_ERR_CUDA;
+  }
+  fn<<<grid, 32, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (prof) {
+    if (cudaEventRecord(e1, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({kind, e0, e1});
+  }
+  return SSM_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
@@ -468,9 +495,164 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
   return rc;
 }
 
+// Gradients of one selective-scan call (bbar_mode 0, time-varying B and C, N <= 16).
+int scan_backward(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                  const float* D, const void* z, const float* delta_bias, const float* h_init,
+                  const void* dout, const float* dfinal, void* dx, void* ddelta, float* dA, float* dB,
+                  float* dC, float* dD, void* dz, float* ddelta_bias, float* dh_init,
+                  const ssm_dims* dims, cudaStream_t stream) {
+  if (!dims) return SSM_ERR_NULL;
+  const ssm_dims d = *dims;
+  if (d.batch <= 0 || d.dim <= 0 || d.dstate <= 0 || d.dstate > 64 || d.seqlen < 0)
+    return SSM_ERR_DIMS;
+  if ((d.io_dtype != SSM_F32 && d.io_dtype != SSM_BF16) ||
+      (d.bc_layout != SSM_BC_TIME_VARYING && d.bc_layout != SSM_BC_PER_CHANNEL) ||
+      (d.delta_softplus != 0 && d.delta_softplus != 1) || (d.state_in != 0 && d.state_in != 1) ||
+      (d.bbar_mode != 0 && d.bbar_mode != 1) || d.reserved != 0)
+    return SSM_ERR_DIMS;
+  if (d.bc_layout != SSM_BC_TIME_VARYING || d.bbar_mode != 0 || d.dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (!A || !dA) return SSM_ERR_NULL;
+  if (d.seqlen > 0 && (!x || !delta || !B || !C || !dout || !dx || !ddelta || !dB || !dC))
+    return SSM_ERR_NULL;
+  if (z && !dz) return SSM_ERR_NULL;
+  const void* ptrs[] = {x, delta, A, B, C, D, z, delta_bias, h_init, dout, dfinal, dx, ddelta,
+                        dA, dB, dC, dD, dz, ddelta_bias, dh_init};
+  for (const void* q : ptrs)
+    if (q && ((uintptr_t)q & 15u)) return SSM_ERR_ALIGN;
+  const size_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
+  const size_t act = (size_t)d.batch * d.seqlen * d.dim * esz;
+  const size_t bcn = (size_t)d.batch * d.seqlen * d.dstate;
+  const size_t st = (size_t)d.batch * d.dim * d.dstate * 4;
+  struct { const void* p; size_t n; } ins[] = {
+      {x, act}, {delta, act}, {A, (size_t)d.dim * d.dstate * 4}, {B, bcn * esz}, {C, bcn * esz},
+      {D, (size_t)d.dim * 4}, {z, act}, {delta_bias, (size_t)d.dim * 4}, {h_init, st}, {dout, act},
+      {dfinal, st}};
+  struct { const void* p; size_t n; } outs[] = {
+      {dx, act}, {ddelta, act}, {dA, (size_t)d.dim * d.dstate * 4}, {dB, bcn * 4}, {dC, bcn * 4},
+      {dD, (size_t)d.dim * 4}, {dz, act}, {ddelta_bias, (size_t)d.dim * 4}, {dh_init, st}};
+  for (auto& o : outs) {
+    for (auto& in : ins)
+      if (overlaps(o.p, o.n, in.p, in.n)) return SSM_ERR_OVERLAP;
+    for (auto& o2 : outs)
+      if (&o2 != &o && overlaps(o.p, o.n, o2.p, o2.n)) return SSM_ERR_OVERLAP;
+  }
+
+  // the shared gradients are sums: start from zero
+  if (cudaMemsetAsync(dA, 0, (size_t)d.dim * d.dstate * 4, stream) != cudaSuccess) return SSM_ERR_CUDA;
+  if (dD && cudaMemsetAsync(dD, 0, (size_t)d.dim * 4, stream) != cudaSuccess) return SSM_ERR_CUDA;
+  if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)d.dim * 4, stream) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (d.seqlen == 0) {
+    // the final state is the initial one
+    if (dh_init) {
+      cudaError_t e = dfinal ? cudaMemcpyAsync(dh_init, dfinal, st, cudaMemcpyDeviceToDevice, stream)
+                             : cudaMemsetAsync(dh_init, 0, st, stream);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+  }
+  if (cudaMemsetAsync(dB, 0, bcn * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(dC, 0, bcn * 4, stream) != cudaSuccess)
+    return SSM_ERR_CUDA;
+
+  const int S = padded_states(d.dstate);
+  const ssm::BwdKernels bk = ssm::lookup_bwd(d.io_dtype == SSM_BF16, S);
+  const ssm::KernelInfo agg = lookup(d.io_dtype, false, S, 1, 0, 0);
+  if (!bk.main || !agg.fn) return SSM_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (d.batch > 65535) return SSM_ERR_DIMS;
+
+  // chunks: one warp per 32 channels and chunk; as many chunks as give 8 warps per SM
+  // (chunks of at least min_chunk_len steps)
+  const unsigned gx = (unsigned)((d.dim + 31) / 32);
+  int64_t k = g_opt_chunks.load();
+  if (k <= 0) {
+    const int64_t warps = d.batch * gx, want = (int64_t)sms * 8;
+    k = warps >= want ? 1 : std::max<int64_t>(1, want / warps);
+    k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / std::max<int64_t>(ssm::kChunkAlign,
+                                                                                 g_opt_min_chunk_len.load())));
+  }
+  k = std::max<int64_t>(1, std::min<int64_t>(k, (d.seqlen + ssm::kChunkAlign - 1) / ssm::kChunkAlign));
+  k = std::min<int64_t>(k, 65535);
+  int64_t len = (d.seqlen + k - 1) / k;
+  len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
+  const int nchunks = (int)((d.seqlen + len - 1) / len);
+
+  const size_t nH = (size_t)(nchunks - 1) * d.batch * d.dim * d.dstate;
+  const size_t nS = (size_t)(nchunks - 1) * d.batch * d.dim;
+  const size_t nck = (size_t)((d.seqlen + bk.seg - 1) / bk.seg) * d.batch * d.dim * S;
+  const size_t bytes = (2 * nH + 2 * nS + nck) * sizeof(float);
+  cudaMemPool_t pool;
+  if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+  void* ws = nullptr;
+  if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+  float* const w0 = static_cast<float*>(ws);
+
+  ssm::BwdParams bp;
+  std::memset(&bp, 0, sizeof bp);
+  bp.x = x; bp.delta = delta; bp.z = z; bp.A = A; bp.B = B; bp.C = C; bp.Dskip = D;
+  bp.bias = delta_bias; bp.h_init = h_init; bp.dout = dout; bp.dfinal = dfinal;
+  bp.dx = dx; bp.ddelta = ddelta; bp.dz = dz; bp.dA = dA; bp.dB = dB; bp.dC = dC; bp.dD = dD;
+  bp.dbias = ddelta_bias; bp.dh_init = dh_init;
+  bp.ws_H = w0; bp.ws_S = w0 + nH; bp.ws_M = w0 + nH + nS; bp.ws_S2 = w0 + 2 * nH + nS;
+  bp.ws_ck = w0 + 2 * nH + 2 * nS;
+  bp.batch = d.batch; bp.seqlen = d.seqlen; bp.dim = d.dim; bp.dstate = (int)d.dstate;
+  bp.nchunks = nchunks; bp.chunk_len = len; bp.delta_softplus = d.delta_softplus;
+
+  int rc = SSM_OK;
+  if (nchunks > 1) {
+    // forward chunk aggregates: the tiled forward kernel's aggregate pass
+    ScanParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.bias = delta_bias; p.h_init = h_init;
+    p.ws_H = w0; p.ws_S = w0 + nH;
+    p.batch = d.batch; p.seqlen = d.seqlen; p.dim = d.dim; p.dstate = (int)d.dstate;
+    p.nchunks = nchunks; p.chunk_len = len; p.delta_softplus = d.delta_softplus;
+    p.pow_path = (int)g_opt_pow_path.load();
+    p.stall_tile = -1;
+    int* status = nullptr;
+    if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) rc = SSM_ERR_CUDA;
+    p.status = status;
+    ssm::TmaMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    const bool tma = g_opt_tma.load() && tma_ok(d);
+    p.use_tma = tma ? 1 : 0;
+    if (rc == SSM_OK && tma) {
+      const int eb = (int)esz;
+      if (!encode3d(&maps.x, x, eb, d.dim, d.seqlen, d.batch, agg.ch, agg.t) ||
+          !encode3d(&maps.delta, delta, eb, d.dim, d.seqlen, d.batch, agg.ch, agg.t) ||
+          !encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, agg.t))
+        rc = SSM_ERR_CUDA;
+    }
+    if (rc == SSM_OK)
+      rc = launch(agg, 0, dim3((unsigned)((d.dim + agg.ch - 1) / agg.ch), (unsigned)(nchunks - 1),
+                               (unsigned)d.batch), maps, p, stream);
+    if (rc == SSM_OK)
+      rc = launch_bwd(bk.reverse_aggregate, 3, dim3(gx, (unsigned)(nchunks - 1), (unsigned)d.batch), bp,
+                      stream);
+  }
+  if (rc == SSM_OK) rc = launch_bwd(bk.main, 4, dim3(gx, (unsigned)nchunks, (unsigned)d.batch), bp, stream);
+  if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
+  return rc;
+}
+
 }  // namespace ssm_internal
 
 extern "C" {
+
+int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, const float* delta_bias,
+                           const float* h_init, const void* dout, const float* dfinal_state,
+                           void* dx, void* ddelta, float* dA, float* dB, float* dC, float* dD,
+                           void* dz, float* ddelta_bias, float* dh_init, const ssm_dims* dims,
+                           cudaStream_t stream) {
+  return ssm_internal::scan_backward(x, delta, A, B, C, D, z, delta_bias, h_init, dout, dfinal_state,
+                                     dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dh_init, dims, stream);
+}
+
 
 int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
                            const void* C, const float* D, const void* z,
@@ -543,8 +725,8 @@ int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, in
     std::lock_guard<std::mutex> lk(g_prof_mu);
     recs.swap(g_prof);
   }
-  int64_t cnt[3] = {0, 0, 0};
-  double ms[3] = {0, 0, 0};
+  int64_t cnt[kKinds] = {};
+  double ms[kKinds] = {};
   int rc = SSM_OK;
   for (auto& r : recs) {
     float t = 0.f;
@@ -557,7 +739,7 @@ int ssm_profile_read(const char** names, int64_t* launches, double* total_ms, in
   }
   if (rc != SSM_OK) return rc;
   int rows = 0;
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < kKinds; ++k) {
     if (!cnt[k]) continue;
     if (rows < max) {
       if (names) names[rows] = kKindName[k];
