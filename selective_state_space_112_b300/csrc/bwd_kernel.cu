@@ -16,10 +16,11 @@
 //    mu = dfinal past the last chunk.
 // bwd_main then sweeps its chunk forward once, storing h every SEG steps (HBM
 // checkpoints), and walks the segments backwards: it rebuilds the segment's states
-// into shared memory and runs the adjoint sweep over them.  dB, dC (summed over
-// channels) leave through a warp reduce-scatter and one atomic add per (t, n) per
-// warp; dA, dD and the bias gradient accumulate in registers and are added once per
-// lane.
+// into shared memory and runs the adjoint sweep over them.  Inputs move in tiles of
+// SEG steps staged in shared memory, all loads of a tile issued together.  dB, dC
+// (summed over channels) leave through a warp reduce-scatter and one atomic add per
+// (t, n) per warp; dA, dD and the bias gradient accumulate in registers and are
+// added once per lane.
 #include <cuda_runtime.h>
 
 #include "bwd_kernel.h"
@@ -28,13 +29,7 @@ namespace ssm {
 
 namespace {
 
-constexpr int SEG = 16;  // steps per rebuilt segment (chunk lengths are multiples of 32)
-
-template <typename IO, int S>
-__device__ __forceinline__ void load_row_g(const void* base, int64_t row, int N, float (&v)[S]) {
-#pragma unroll
-  for (int n = 0; n < S; ++n) v[n] = n < N ? IO::load(base, row * N + n) : 0.f;
-}
+constexpr int SEG = 8;  // steps per tile and per rebuilt segment (chunks are multiples of 32)
 
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
 
@@ -53,11 +48,104 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// The inputs of SEG steps in shared memory: one column per lane (channel) for the
+// per-(step, channel) values, one row per step for B and C (shared by the channels).
+// All loads of a tile are issued before any step uses them.
+template <int S>
+struct Tile {
+  float v[SEG][32];  // delta + bias
+  float x[SEG][32];
+  float g[SEG][32];  // dout
+  float z[SEG][32];
+  float b[SEG][S];   // zero past N
+  float c[SEG][S];
+};
+
+// A tile's inputs in flight: issued into registers one tile ahead, stored to shared
+// memory when the tile is reached (the loads overlap the previous tile's compute).
+template <int S>
+struct TileRegs {
+  static constexpr int RPL = (SEG * S + 31) / 32;  // B / C row values per lane
+  float v[SEG], x[SEG], g[SEG], z[SEG];
+  float b[RPL], c[RPL];
+};
+
+template <typename IO, int S, bool X, bool G, bool BROW, bool CROW>
+__device__ __forceinline__ void fetch_tile(TileRegs<S>& r, const BwdParams& p, int b, int64_t ts, int cnt,
+                                           int64_t dd, int lane) {
+  const int64_t L = p.seqlen, Dm = p.dim;
+#pragma unroll
+  for (int k = 0; k < SEG; ++k) {
+    if (k < cnt) {
+      const int64_t i = ((int64_t)b * L + ts + k) * Dm + dd;
+      r.v[k] = IO::load(p.delta, i);
+      if (X) r.x[k] = IO::load(p.x, i);
+      if (G) {
+        r.g[k] = IO::load(p.dout, i);
+        if (p.z) r.z[k] = IO::load(p.z, i);
+      }
+    }
+  }
+  if (BROW || CROW) {
+    const int N = p.dstate;
+#pragma unroll
+    for (int m = 0; m < TileRegs<S>::RPL; ++m) {
+      const int e = lane + 32 * m;
+      if (e < cnt * N) {
+        const int k = e / N, n = e - k * N;
+        const int64_t row = ((int64_t)b * L + ts + k) * N + n;
+        if (BROW) r.b[m] = IO::load(p.B, row);
+        if (CROW) r.c[m] = IO::load(p.C, row);
+      }
+    }
+  }
+}
+
+template <int S, bool X, bool G, bool BROW, bool CROW>
+__device__ __forceinline__ void stash_tile(const TileRegs<S>& r, Tile<S>& tl, const BwdParams& p, int cnt,
+                                           float biasv, int lane) {
+  __syncwarp();  // every lane is done with the previous tile
+#pragma unroll
+  for (int k = 0; k < SEG; ++k) {
+    if (k < cnt) {
+      tl.v[k][lane] = r.v[k] + biasv;
+      if (X) tl.x[k][lane] = r.x[k];
+      if (G) {
+        tl.g[k][lane] = r.g[k];
+        if (p.z) tl.z[k][lane] = r.z[k];
+      }
+    }
+  }
+  if (BROW || CROW) {
+    const int N = p.dstate;
+#pragma unroll
+    for (int m = 0; m < TileRegs<S>::RPL; ++m) {
+      const int e = lane + 32 * m;
+      if (e < cnt * N) {
+        const int k = e / N, n = e - k * N;
+        if (BROW) tl.b[k][n] = r.b[m];
+        if (CROW) tl.c[k][n] = r.c[m];
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <int S>
+__device__ __forceinline__ void zero_rows(Tile<S>& tl, int lane) {
+  for (int e = lane; e < SEG * S; e += 32) {
+    (&tl.b[0][0])[e] = 0.f;
+    (&tl.c[0][0])[e] = 0.f;
+  }
+  __syncwarp();
+}
+
 }  // namespace
 
 // Reverse chunk aggregates of chunks 1 .. nchunks-1 (grid.y = chunk - 1).
 template <typename IO, int S>
 __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
+  __shared__ Tile<S> tl;
   const int lane = threadIdx.x;
   const int64_t L = p.seqlen, Dm = p.dim;
   const int N = p.dstate;
@@ -66,6 +154,7 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
   const bool valid = d < Dm;
   const int64_t dd = valid ? d : Dm - 1;
   const int64_t t0 = (int64_t)chunk * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const bool sp = p.delta_softplus != 0;
   float A2[S], m[S];
 #pragma unroll
   for (int n = 0; n < S; ++n) {
@@ -73,18 +162,42 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
     m[n] = 0.f;
   }
   const float biasv = p.bias ? p.bias[dd] : 0.f;
+  zero_rows(tl, lane);
   float Ssum = 0.f, Scomp = 0.f;
-  for (int64_t t = t1 - 1; t >= t0; --t) {
-    const int64_t i = ((int64_t)b * L + t) * Dm + dd;
-    const float v = IO::load(p.delta, i) + biasv;
-    const float dt = p.delta_softplus ? softplus<std::is_same<IO, F32>::value>(v) : v;
-    const float g = IO::load(p.dout, i);
-    const float gy = p.z ? g * silu(IO::load(p.z, i)) : g;
-    float c[S];
-    load_row_g<IO, S>(p.C, (int64_t)b * L + t, N, c);
+  const int ntile = (int)((t1 - t0 + SEG - 1) / SEG);
+  auto tile_at = [&](int j, int64_t& ts, int& cnt) {
+    ts = t0 + (int64_t)j * SEG;
+    cnt = (int)min((int64_t)SEG, t1 - ts);
+  };
+  TileRegs<S> rg;
+  {
+    int64_t ts;
+    int cnt;
+    tile_at(ntile - 1, ts, cnt);
+    fetch_tile<IO, S, false, true, false, true>(rg, p, b, ts, cnt, dd, lane);
+  }
+  for (int j = ntile - 1; j >= 0; --j) {
+    int64_t ts;
+    int cnt;
+    tile_at(j, ts, cnt);
+    stash_tile<S, false, true, false, true>(rg, tl, p, cnt, biasv, lane);
+    if (j > 0) {  // the next tile's loads overlap this tile's steps
+      int64_t tn;
+      int cn;
+      tile_at(j - 1, tn, cn);
+      fetch_tile<IO, S, false, true, false, true>(rg, p, b, tn, cn, dd, lane);
+    }
+    float tsum = 0.f;
+    for (int k = cnt - 1; k >= 0; --k) {
+      const float v = tl.v[k][lane];
+      const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
+      const float g = tl.g[k][lane];
+      const float gy = p.z ? g * silu(tl.z[k][lane]) : g;
 #pragma unroll
-    for (int n = 0; n < S; ++n) m[n] = ex2(dt * A2[n]) * fmaf(c[n], gy, m[n]);
-    kahan_add(Ssum, Scomp, dt);
+      for (int n = 0; n < S; ++n) m[n] = ex2(dt * A2[n]) * fmaf(tl.c[k][n], gy, m[n]);
+      tsum += dt;
+    }
+    kahan_add(Ssum, Scomp, tsum);
   }
   if (!valid) return;
   const int64_t ci = ((int64_t)(chunk - 1) * p.batch + b) * Dm + d;
@@ -97,7 +210,8 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
 template <typename IO, int S>
 __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
   __shared__ float hist[SEG + 1][S][32];  // row 0: state before the segment
-  __shared__ float dts[SEG][32], vs[SEG][32];
+  __shared__ float dts[SEG][32];
+  __shared__ Tile<S> tl;
   const int lane = threadIdx.x;
   const int64_t L = p.seqlen, Dm = p.dim;
   const int N = p.dstate;
@@ -114,6 +228,7 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
   const float biasv = p.bias ? p.bias[dd] : 0.f;
   const float Dv = p.Dskip ? p.Dskip[dd] : 0.f;
   const int64_t sidx = ((int64_t)b * Dm + dd) * N;
+  zero_rows(tl, lane);
 
   // ---- state at the chunk start (forward carry)
   float h[S];
@@ -138,23 +253,45 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
       if (n < N) kap[n] = fmaf(ex2(Sc * A2[n]), kap[n], p.ws_M[ci * N + n]);
   }
 
-  // ---- forward sweep: checkpoints at every segment start
+  // ---- forward sweep: a checkpoint at every segment start
   const int nseg = (int)((t1 - t0 + SEG - 1) / SEG);
   const int64_t seg0 = t0 / SEG;
-  for (int64_t t = t0; t < t1; ++t) {
-    if ((t - t0) % SEG == 0 && valid) {
-      float* ck = p.ws_ck + (((seg0 + (t - t0) / SEG) * p.batch + b) * Dm + d) * S;
+  auto seg_at = [&](int j, int64_t& ts, int& cnt) {
+    ts = t0 + (int64_t)j * SEG;
+    cnt = (int)min((int64_t)SEG, t1 - ts);
+  };
+  TileRegs<S> rg;
+  {
+    int64_t ts;
+    int cnt;
+    seg_at(0, ts, cnt);
+    fetch_tile<IO, S, true, false, true, false>(rg, p, b, ts, cnt, dd, lane);
+  }
+  for (int j = 0; j < nseg; ++j) {
+    int64_t ts;
+    int cnt;
+    seg_at(j, ts, cnt);
+    if (valid) {
+      float* ck = p.ws_ck + (((seg0 + j) * p.batch + b) * Dm + d) * S;
 #pragma unroll
       for (int n = 0; n < S; ++n) ck[n] = h[n];
     }
-    const int64_t i = ((int64_t)b * L + t) * Dm + dd;
-    const float v = IO::load(p.delta, i) + biasv;
-    const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
-    const float u = dt * IO::load(p.x, i);
-    float bv[S];
-    load_row_g<IO, S>(p.B, (int64_t)b * L + t, N, bv);
+    stash_tile<S, true, false, true, false>(rg, tl, p, cnt, biasv, lane);
+    if (j + 1 < nseg) {
+      int64_t tn;
+      int cn;
+      seg_at(j + 1, tn, cn);
+      fetch_tile<IO, S, true, false, true, false>(rg, p, b, tn, cn, dd, lane);
+    } else {  // the reverse walk starts with the last segment
+      fetch_tile<IO, S, true, true, true, true>(rg, p, b, ts, cnt, dd, lane);
+    }
+    for (int k = 0; k < cnt; ++k) {
+      const float v = tl.v[k][lane];
+      const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
+      const float u = dt * tl.x[k][lane];
 #pragma unroll
-    for (int n = 0; n < S; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], u * bv[n]);
+      for (int n = 0; n < S; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], u * tl.b[k][n]);
+    }
   }
 
   // ---- segments in reverse: rebuild the states, then the adjoint sweep
@@ -163,57 +300,58 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
   for (int n = 0; n < S; ++n) gA[n] = 0.f;
   float gD = 0.f, gbias = 0.f;
   for (int j = nseg - 1; j >= 0; --j) {
-    const int64_t ts = t0 + (int64_t)j * SEG, te = min(ts + SEG, t1);
-    const int cnt = (int)(te - ts);
-    __syncwarp();  // the previous segment's readers are done with the buffers
+    int64_t ts;
+    int cnt;
+    seg_at(j, ts, cnt);
     {
       const float* ck = p.ws_ck + (((seg0 + j) * p.batch + b) * Dm + dd) * S;
 #pragma unroll
       for (int n = 0; n < S; ++n) h[n] = valid ? ck[n] : 0.f;
     }
+    stash_tile<S, true, true, true, true>(rg, tl, p, cnt, biasv, lane);
+    if (j > 0) {
+      int64_t tn;
+      int cn;
+      seg_at(j - 1, tn, cn);
+      fetch_tile<IO, S, true, true, true, true>(rg, p, b, tn, cn, dd, lane);
+    }
 #pragma unroll
     for (int n = 0; n < S; ++n) hist[0][n][lane] = h[n];
     for (int k = 0; k < cnt; ++k) {
-      const int64_t i = ((int64_t)b * L + ts + k) * Dm + dd;
-      const float v = IO::load(p.delta, i) + biasv;
+      const float v = tl.v[k][lane];
       const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
       dts[k][lane] = dt;
-      vs[k][lane] = v;
-      const float u = dt * IO::load(p.x, i);
-      float bv[S];
-      load_row_g<IO, S>(p.B, (int64_t)b * L + ts + k, N, bv);
+      const float u = dt * tl.x[k][lane];
 #pragma unroll
       for (int n = 0; n < S; ++n) {
-        h[n] = fmaf(ex2(dt * A2[n]), h[n], u * bv[n]);
+        h[n] = fmaf(ex2(dt * A2[n]), h[n], u * tl.b[k][n]);
         hist[k + 1][n][lane] = h[n];
       }
     }
     for (int k = cnt - 1; k >= 0; --k) {
       const int64_t t = ts + k;
       const int64_t i = ((int64_t)b * L + t) * Dm + dd;
-      const float dt = dts[k][lane], v = vs[k][lane];
-      const float xv = IO::load(p.x, i), g = IO::load(p.dout, i);
+      const float dt = dts[k][lane], v = tl.v[k][lane];
+      const float xv = tl.x[k][lane], g = tl.g[k][lane];
       float zv = 0.f, sz = 1.f;
       if (p.z) {
-        zv = IO::load(p.z, i);
+        zv = tl.z[k][lane];
         sz = sigmoidf_(zv);
       }
       const float gy = p.z ? g * zv * sz : g;
-      float bv[S], cv[S];
-      load_row_g<IO, S>(p.B, (int64_t)b * L + t, N, bv);
-      load_row_g<IO, S>(p.C, (int64_t)b * L + t, N, cv);
       float ddt = 0.f, gx = 0.f, y = 0.f;
       float red[32];
 #pragma unroll
       for (int n = 0; n < S; ++n) {
         const float a = ex2(dt * A2[n]);
         const float hp = hist[k][n][lane], hc = hist[k + 1][n][lane];
-        const float lam = fmaf(cv[n], gy, kap[n]);
+        const float bn = tl.b[k][n], cn = tl.c[k][n];
+        const float lam = fmaf(cn, gy, kap[n]);
         const float ga = lam * hp * a;  // gradient of a_t, times a_t
         gA[n] = fmaf(ga, dt, gA[n]);
-        ddt = fmaf(ga, A2[n] * kLn2, fmaf(lam, bv[n] * xv, ddt));
-        gx = fmaf(lam, bv[n], gx);
-        y = fmaf(cv[n], hc, y);
+        ddt = fmaf(ga, A2[n] * kLn2, fmaf(lam, bn * xv, ddt));
+        gx = fmaf(lam, bn, gx);
+        y = fmaf(cn, hc, y);
         red[n] = valid ? lam * dt * xv : 0.f;       // this channel's share of dB
         red[16 + n] = valid ? gy * hc : 0.f;        // and of dC
         kap[n] = a * lam;
