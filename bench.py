@@ -244,6 +244,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--conv", action="store_true",
                     help="the Mamba-block prologue (causal conv of width 4 + silu) fused in")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (gradients of every input) instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -271,6 +273,8 @@ def main():
     spec["seed"] = spec["seed"] + 1000 * rank  # independent replica per rank
     w = make_workload(args.workload, **spec)
     t = device_tensors(w, torch, device)
+    if args.backward:
+        return backward_bench(args, w, t, world, rank, local, device, dist, torch, ssm)
     out = torch.empty_like(t["x"])
     fs0 = t["h0"]
     fs = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=device)
@@ -418,6 +422,171 @@ def main():
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+# The main backward kernel forms Abar three times per state update (the checkpoint
+# sweep, the segment rebuild and the adjoint sweep): its MUFU ex2 roofline.
+BWD_EX2_PER_UPDATE = 3
+
+
+def backward_bench(args, w, t, world, rank, local, device, dist, torch, ssm):
+    """One step = one ssm_selective_scan_bwd call over the whole workload, with a
+    seeded upstream gradient dout ~ N(0, 1) in the io dtype."""
+    from selective_state_space_112_b300.workloads import f32_to_bf16_bits
+    rng = np.random.default_rng(w.seed + 4242)
+    dout = rng.standard_normal(w.x.shape, dtype=np.float32)
+    if w.io == "bf16":
+        dout = f32_to_bf16_bits(dout)
+    t["dout"] = (torch.from_numpy(dout.view(np.int16)).view(torch.bfloat16) if w.io == "bf16"
+                 else torch.from_numpy(dout)).to(device)
+    stream = torch.cuda.current_stream(device)
+    grads = ssm.ssm_selective_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                       t["delta_bias"], t["h0"], t["dout"],
+                                       delta_softplus=w.delta_softplus)
+
+    def bwd(x, delta, A, B, C, D, z, bias, h0, dout_):
+        ssm.ssm_selective_scan_bwd(x, delta, A, B, C, D, z, bias, h0, dout_,
+                                   delta_softplus=w.delta_softplus, grads=grads)
+
+    def step():
+        bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], t["h0"], t["dout"])
+
+    for _ in range(args.warmup):
+        step()
+    assert ssm.ssm_check_status() == 0
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ssm.ssm_kernel_launches()
+    ssm.ssm_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ssm.ssm_profile_enable(False)
+    prof = ssm.ssm_profile_read()
+    launches = ssm.ssm_kernel_launches() - launches0
+    assert ssm.ssm_check_status() == 0
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        ms = max_over_ranks(ms, dist, device)
+        dist.barrier()
+    ms_step = ms / args.steps
+    units = w.tokens_channels
+    value = job_throughput(units, args.steps, ms, world)
+
+    hbm_peak, sm_max, peak_kind = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    esz = 2 if w.io == "bf16" else 4
+    bt = w.batch * w.seqlen
+    # inputs x, delta, z, dout and outputs dx, ddelta, dz per (b, t, d); B, C in and
+    # dB, dC (fp32) out per (b, t, n); A, D, bias and their gradients per channel
+    per_tc = 7 if w.z is not None else 5  # (x, delta, [z], dout) in, (dx, ddelta, [dz]) out
+    alg = units * esz * per_tc + bt * w.dstate * (2 * esz + 8) + w.dim * (w.dstate + 2) * 8
+    dom = max(prof, key=lambda k: prof[k][1]) if prof else None
+    dom_ms = prof[dom][1] / prof[dom][0] if dom else ms_step
+    total_ms = sum(v[1] for v in prof.values()) or 1.0
+    upd_peak = EX2_PER_SM_CLK / BWD_EX2_PER_UPDATE * sms * sm_max * 1e6 / 1e9
+    upd_achieved = w.element_updates / (dom_ms * 1e-3) / 1e9
+    hbm_achieved = alg / (dom_ms * 1e-3) / 1e9
+    roof = {"bound": "alu", "kernel": dom, "achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
+            "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
+            "peak_basis": (f"{EX2_PER_SM_CLK} MUFU ex2 per SM per clock (measured on B300) / "
+                           f"{BWD_EX2_PER_UPDATE} ex2 per state update in the main backward kernel x "
+                           f"{sms} SMs x {sm_max:.0f} MHz"),
+            "traffic": None, "algorithmic_bytes_per_launch": alg, "kernel_ms_avg": round(dom_ms, 4),
+            "hbm": {"achieved": round(hbm_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(hbm_achieved / hbm_peak, 4), "peak_source": peak_kind},
+            "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4),
+                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()}}
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic",
+           "config": {"workload": args.workload, "pass": "backward", "batch": w.batch,
+                      "seqlen": w.seqlen, "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io,
+                      "gate": w.z is not None, "state_in": w.h0 is not None,
+                      "parallelism": f"replica x{world}" if world > 1 else "single",
+                      "l2": f"inputs {alg / 1e9:.2f} GB > 126 MB L2; no flush needed"
+                            if alg > 4 * 126e6 else "L2 resident (latency case)"},
+           "hbm_gbs_step": round(alg / (ms_step * 1e-3) / 1e9, 1),
+           "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary()}
+
+    if not args.no_e2e:
+        names = ("x", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0", "dout")
+        host = {k: (t[k].cpu().pin_memory() if t[k] is not None else None) for k in names}
+        dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items() if k in names}
+        outs = {k: v for k, v in grads.items() if v is not None}
+        outs_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            bwd(*[dev_in[k] for k in names])
+            for k, v in outs.items():
+                outs_h[k].copy_(v, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            ems = max_over_ranks(ems, dist, device)
+        res["e2e"] = {"value": job_throughput(units, args.e2e_steps, ems, world), "unit": UNIT,
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": ems / args.e2e_steps}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_bwd(w, dout)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def cpu_baseline_bwd(w, dout, budget_s: float = 15.0):
+    """The float64 oracle's backward on channels 0..k-1 of batch row 0, whole sequence."""
+    import oracle
+    from selective_state_space_112_b300.workloads import bf16_bits_to_f32
+    cores = oracle.max_threads()
+    g64 = bf16_bits_to_f32(dout).astype(np.float64) if w.io == "bf16" else dout.astype(np.float64)
+
+    def run(k):
+        sl = lambda a: None if a is None else np.ascontiguousarray(a[:1, :, :k])
+        ch = lambda a: None if a is None else np.ascontiguousarray(a[:k])
+        args = (sl(w.x), sl(w.delta), ch(w.A), np.ascontiguousarray(w.B[:1]), np.ascontiguousarray(w.C[:1]),
+                ch(w.D), sl(w.z), ch(w.delta_bias),
+                None if w.h0 is None else np.ascontiguousarray(w.h0[:1, :k]))
+        gs = sl(g64)
+        t0 = time.perf_counter()
+        oracle.selective_scan_bwd(*args, dout=gs, delta_softplus=w.delta_softplus, io_dtype=w.io)
+        return time.perf_counter() - t0
+
+    cap = min(w.dim, 512)
+    k = min(cap, max(cores, 8))
+    t = run(k)
+    k2 = int(min(cap, max(k, k * budget_s / max(t, 1e-3))))
+    k2 = max(1, (k2 // cores) * cores) if k2 >= cores else k2
+    if k2 > k:
+        t, k = run(k2), k2
+    units = k * w.seqlen
+    return {"value": units / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"backward, channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, N={w.dstate} "
+                      f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
 
 
 def reference_arm(args, world, rank):

@@ -77,7 +77,7 @@ def ssm_conv_selective_scan_fwd(x, conv_w, conv_b, conv_state, delta, A, B, C, D
 
 
 def ssm_selective_scan_bwd(x, delta, A, B, C, D, z, delta_bias, h_init, dout, dfinal_state=None,
-                           *, delta_softplus: bool = True, stream=None):
+                           *, delta_softplus: bool = True, stream=None, grads=None):
     """Gradients of ``ssm_selective_scan_fwd`` (time-varying B, C; bbar_mode 0).
 
     Inputs as the forward (h_init: (batch, dim, N) float32 or None); dout: gradient of
@@ -85,7 +85,8 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, D, z, delta_bias, h_init, dout, df
     or None.  Returns a dict: dx, ddelta, dz (io dtype; dz None without a gate),
     dA (dim, N), dB, dC (batch, L, N), dD, ddelta_bias (dim,), dh_init (batch, dim, N)
     -- all float32 except dx, ddelta, dz; dD / ddelta_bias / dh_init are None when D /
-    delta_bias / h_init are.
+    delta_bias / h_init are.  ``grads``: such a dict from an earlier call with the same
+    shapes, whose tensors are overwritten instead of allocating new ones.
     """
     torch = _torch()
     if x.dtype == torch.float32:
@@ -111,7 +112,7 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, D, z, delta_bias, h_init, dout, df
         if not t.is_contiguous() or not t.is_cuda:
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     f32 = dict(dtype=torch.float32, device=x.device)
-    g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+    g = grads if grads is not None else {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
          "dz": torch.empty_like(x) if z is not None else None,
          "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, L, N), **f32),
          "dC": torch.empty((batch, L, N), **f32),
