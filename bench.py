@@ -43,21 +43,26 @@ UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDA
 # per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
 # on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (mean of 5 output launches: 256.71 MB read + 58.67 MB write),
+    # long_bf16_16k capture (mean of 5 output launches: 256.69 MB read + 58.85 MB write),
     # scaled by the units processed (x8) to the 131072-step workload
-    "long_bf16": {"bytes_per_launch": 2523000000, "kernel_src_sha": "28618117746fe831"},
-    "long_bf16_16k": {"bytes_per_launch": 315380000, "kernel_src_sha": "28618117746fe831"},
+    "long_bf16": {"bytes_per_launch": 2524000000, "kernel_src_sha": "ec0c843f3995e92e"},
+    "long_bf16_16k": {"bytes_per_launch": 315540000, "kernel_src_sha": "ec0c843f3995e92e"},
 }
 
 
 def kernel_src_sha() -> str:
+    """Hash of the sources of the tiled forward kernels and their launch (the kernel
+    the recorded traffic belongs to): scan_tile.cuh, kernel_table.cuh, the
+    kernels_*.cu instantiations and ssm_scan.cu."""
     import glob
     import hashlib
+    csrc = os.path.join(ROOT, "selective_state_space_112_b300", "csrc")
+    files = ([os.path.join(csrc, n) for n in ("scan_tile.cuh", "kernel_table.cuh", "ssm_scan.cu")]
+             + glob.glob(os.path.join(csrc, "kernels_*.cu")))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_112_b300", "csrc", "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(f, "rb") as fh:
-                h.update(os.path.basename(f).encode() + fh.read())
+    for f in sorted(files):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
