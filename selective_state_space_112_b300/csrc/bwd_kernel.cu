@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
 
 template <typename IO, int S>
 __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
-  __shared__ float hist[SEG + 1][S][32];  // row 0: state before the segment
+  __shared__ float2 hist[SEG + 1][S / 2][32];  // state pairs; row 0: state before the segment
   __shared__ float dts[SEG][32];
   __shared__ Tile<S> tl;
   const int lane = threadIdx.x;
@@ -225,8 +225,12 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
   float A2[S];
 #pragma unroll
   for (int n = 0; n < S; ++n) A2[n] = n < N ? p.A[dd * N + n] * kLog2e : 0.f;
+  float2 A2p[S / 2];  // the same, as state pairs for the f32x2 operations
+#pragma unroll
+  for (int i = 0; i < S / 2; ++i) A2p[i] = make_float2(A2[2 * i], A2[2 * i + 1]);
   const float biasv = p.bias ? p.bias[dd] : 0.f;
   const float Dv = p.Dskip ? p.Dskip[dd] : 0.f;
+  const float vm = valid ? 1.f : 0.f;  // absent channels add nothing to dB, dC
   const int64_t sidx = ((int64_t)b * Dm + dd) * N;
   zero_rows(tl, lane);
 
@@ -289,24 +293,36 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
       const float v = tl.v[k][lane];
       const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
       const float u = dt * tl.x[k][lane];
+      const float2 dt2 = make_float2(dt, dt), u2 = make_float2(u, u);
 #pragma unroll
-      for (int n = 0; n < S; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], u * tl.b[k][n]);
+      for (int i = 0; i < S / 2; ++i) {
+        const float2 e = __fmul2_rn(dt2, A2p[i]);
+        const float2 bb = __fmul2_rn(u2, *reinterpret_cast<const float2*>(&tl.b[k][2 * i]));
+        const float2 hh = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), make_float2(h[2 * i], h[2 * i + 1]), bb);
+        h[2 * i] = hh.x;
+        h[2 * i + 1] = hh.y;
+      }
     }
   }
 
   // ---- segments in reverse: rebuild the states, then the adjoint sweep
-  float gA[S];
+  float2 gA2[S / 2], kap2[S / 2];
 #pragma unroll
-  for (int n = 0; n < S; ++n) gA[n] = 0.f;
+  for (int i = 0; i < S / 2; ++i) {
+    gA2[i] = make_float2(0.f, 0.f);
+    kap2[i] = make_float2(kap[2 * i], kap[2 * i + 1]);
+  }
   float gD = 0.f, gbias = 0.f;
   for (int j = nseg - 1; j >= 0; --j) {
     int64_t ts;
     int cnt;
     seg_at(j, ts, cnt);
+    float2 h2[S / 2];
     {
       const float* ck = p.ws_ck + (((seg0 + j) * p.batch + b) * Dm + dd) * S;
 #pragma unroll
-      for (int n = 0; n < S; ++n) h[n] = valid ? ck[n] : 0.f;
+      for (int i = 0; i < S / 2; ++i)
+        h2[i] = valid ? make_float2(ck[2 * i], ck[2 * i + 1]) : make_float2(0.f, 0.f);
     }
     stash_tile<S, true, true, true, true>(rg, tl, p, cnt, biasv, lane);
     if (j > 0) {
@@ -316,21 +332,24 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
       fetch_tile<IO, S, true, true, true, true>(rg, p, b, tn, cn, dd, lane);
     }
 #pragma unroll
-    for (int n = 0; n < S; ++n) hist[0][n][lane] = h[n];
+    for (int i = 0; i < S / 2; ++i) hist[0][i][lane] = h2[i];
     for (int k = 0; k < cnt; ++k) {
       const float v = tl.v[k][lane];
       const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
       dts[k][lane] = dt;
       const float u = dt * tl.x[k][lane];
+      const float2 dt2 = make_float2(dt, dt), u2 = make_float2(u, u);
 #pragma unroll
-      for (int n = 0; n < S; ++n) {
-        h[n] = fmaf(ex2(dt * A2[n]), h[n], u * tl.b[k][n]);
-        hist[k + 1][n][lane] = h[n];
+      for (int i = 0; i < S / 2; ++i) {
+        const float2 e = __fmul2_rn(dt2, A2p[i]);
+        const float2 bb = __fmul2_rn(u2, *reinterpret_cast<const float2*>(&tl.b[k][2 * i]));
+        h2[i] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[i], bb);
+        hist[k + 1][i][lane] = h2[i];
       }
     }
     for (int k = cnt - 1; k >= 0; --k) {
       const int64_t t = ts + k;
-      const int64_t i = ((int64_t)b * L + t) * Dm + dd;
+      const int64_t i0 = ((int64_t)b * L + t) * Dm + dd;
       const float dt = dts[k][lane], v = tl.v[k][lane];
       const float xv = tl.x[k][lane], g = tl.g[k][lane];
       float zv = 0.f, sz = 1.f;
@@ -339,39 +358,59 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
         sz = sigmoidf_(zv);
       }
       const float gy = p.z ? g * zv * sz : g;
-      float ddt = 0.f, gx = 0.f, y = 0.f;
+      const float2 dt2 = make_float2(dt, dt), gy2 = make_float2(gy, gy);
+      const float2 dtx2 = make_float2(dt * xv * vm, dt * xv * vm), gyv2 = make_float2(gy * vm, gy * vm);
+      float2 sA = make_float2(0.f, 0.f), sB = make_float2(0.f, 0.f), y2 = make_float2(0.f, 0.f);
       float red[32];
 #pragma unroll
-      for (int n = 0; n < S; ++n) {
-        const float a = ex2(dt * A2[n]);
-        const float hp = hist[k][n][lane], hc = hist[k + 1][n][lane];
-        const float bn = tl.b[k][n], cn = tl.c[k][n];
-        const float lam = fmaf(cn, gy, kap[n]);
-        const float ga = lam * hp * a;  // gradient of a_t, times a_t
-        gA[n] = fmaf(ga, dt, gA[n]);
-        ddt = fmaf(ga, A2[n] * kLn2, fmaf(lam, bn * xv, ddt));
-        gx = fmaf(lam, bn, gx);
-        y = fmaf(cn, hc, y);
-        red[n] = valid ? lam * dt * xv : 0.f;       // this channel's share of dB
-        red[16 + n] = valid ? gy * hc : 0.f;        // and of dC
-        kap[n] = a * lam;
+      for (int i = 0; i < S / 2; ++i) {
+        const float2 e = __fmul2_rn(dt2, A2p[i]);
+        const float2 a = make_float2(ex2(e.x), ex2(e.y));
+        const float2 hp = hist[k][i][lane], hc = hist[k + 1][i][lane];
+        const float2 bn = *reinterpret_cast<const float2*>(&tl.b[k][2 * i]);
+        const float2 cn = *reinterpret_cast<const float2*>(&tl.c[k][2 * i]);
+        const float2 lam = __ffma2_rn(cn, gy2, kap2[i]);
+        const float2 ga = __fmul2_rn(__fmul2_rn(lam, hp), a);  // gradient of a_t, times a_t
+        gA2[i] = __ffma2_rn(ga, dt2, gA2[i]);
+        sA = __ffma2_rn(ga, A2p[i], sA);   // sum of ga A log2(e)
+        sB = __ffma2_rn(lam, bn, sB);      // sum of lam B
+        y2 = __ffma2_rn(cn, hc, y2);
+        const float2 tb = __fmul2_rn(lam, dtx2), tc = __fmul2_rn(gyv2, hc);
+        red[2 * i] = tb.x;                 // this channel's shares of dB
+        red[2 * i + 1] = tb.y;
+        red[16 + 2 * i] = tc.x;            // and of dC
+        red[16 + 2 * i + 1] = tc.y;
+        kap2[i] = __fmul2_rn(a, lam);
       }
 #pragma unroll
       for (int n = S; n < 16; ++n) red[n] = red[16 + n] = 0.f;
-      gx = fmaf(gy, Dv, gx * dt);
-      y = fmaf(Dv, xv, y);
+      const float lamB = sB.x + sB.y;
+      const float gx = fmaf(gy, Dv, lamB * dt);
+      const float y = fmaf(Dv, xv, y2.x + y2.y);
+      const float ddt = fmaf(sA.x + sA.y, kLn2, lamB * xv);
       const float dv = sp ? ddt * sigmoidf_(v) : ddt;
       gbias += dv;
       gD = fmaf(gy, xv, gD);
       if (valid) {
-        IO::store(p.dx, i, gx);
-        IO::store(p.ddelta, i, dv);
-        if (p.z) IO::store(p.dz, i, g * y * sz * fmaf(zv, 1.f - sz, 1.f));
+        IO::store(p.dx, i0, gx);
+        IO::store(p.ddelta, i0, dv);
+        if (p.z) IO::store(p.dz, i0, g * y * sz * fmaf(zv, 1.f - sz, 1.f));
       }
       const float tot = reduce_scatter32(red, lane);
       const int n = lane & 15;
       if (n < N) atomicAdd((lane < 16 ? p.dB : p.dC) + ((int64_t)b * L + t) * N + n, tot);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < S / 2; ++i) {
+    kap[2 * i] = kap2[i].x;
+    kap[2 * i + 1] = kap2[i].y;
+  }
+  float gA[S];
+#pragma unroll
+  for (int i = 0; i < S / 2; ++i) {
+    gA[2 * i] = gA2[i].x;
+    gA[2 * i + 1] = gA2[i].y;
   }
   if (!valid) return;
   // kap = a_{t0} lam_{t0}: the gradient of the state before the chunk
