@@ -10,10 +10,11 @@
 // carries in both directions use the associative combine of the per-step maps:
 //  * forward: the aggregate pass of the forward kernel (chunk end state from a zero
 //    start, chunk step sum S_c) gives h at each chunk start, h <- exp(A S_c) h + H_c;
-//  * reverse: bwd_reverse_aggregate gives each chunk's adjoint carry from a zero
-//    start at its end, M_c = sum_s (prod_{r=t0..s} a_r) C_s gy_s, and its own S_c; the
-//    carry into chunk c from the right is mu_c = M_{c+1} + exp(A S_{c+1}) mu_{c+1},
-//    mu = dfinal past the last chunk.
+//  * reverse: bwd_reverse_aggregate gives the adjoint carry of each sub-chunk (rsub
+//    per chunk, for more warps) from a zero start at its end,
+//    M = sum_s (prod_{r=t0..s} a_r) C_s gy_s, and its step sum S; the carry into a
+//    chunk from the right folds the later sub-chunks, mu <- M + exp(A S) mu, from
+//    mu = dfinal past the sequence end.
 // bwd_main then sweeps its chunk forward once, storing h every SEG steps (HBM
 // checkpoints), and walks the segments backwards: it rebuilds the segment's states
 // into shared memory and runs the adjoint sweep over them.  Inputs move in tiles of
@@ -142,18 +143,19 @@ __device__ __forceinline__ void zero_rows(Tile<S>& tl, int lane) {
 
 }  // namespace
 
-// Reverse chunk aggregates of chunks 1 .. nchunks-1 (grid.y = chunk - 1).
+// Reverse aggregates of the sub-chunks of chunks 1 .. nchunks-1 (rsub per chunk,
+// grid.y = sub-chunk index - rsub); a sub-chunk past the sequence end is empty.
 template <typename IO, int S>
 __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
   __shared__ Tile<S> tl;
   const int lane = threadIdx.x;
   const int64_t L = p.seqlen, Dm = p.dim;
   const int N = p.dstate;
-  const int b = blockIdx.z, chunk = blockIdx.y + 1;
+  const int b = blockIdx.z, sub = blockIdx.y + p.rsub;
   const int64_t d = (int64_t)blockIdx.x * 32 + lane;
   const bool valid = d < Dm;
   const int64_t dd = valid ? d : Dm - 1;
-  const int64_t t0 = (int64_t)chunk * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const int64_t t0 = min((int64_t)sub * p.rsub_len, L), t1 = min(t0 + p.rsub_len, L);
   const bool sp = p.delta_softplus != 0;
   float A2[S], m[S];
 #pragma unroll
@@ -193,14 +195,22 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
       const float dt = sp ? softplus<std::is_same<IO, F32>::value>(v) : v;
       const float g = tl.g[k][lane];
       const float gy = p.z ? g * silu(tl.z[k][lane]) : g;
+      const float2 dt2 = make_float2(dt, dt), gy2 = make_float2(gy, gy);
 #pragma unroll
-      for (int n = 0; n < S; ++n) m[n] = ex2(dt * A2[n]) * fmaf(tl.c[k][n], gy, m[n]);
+      for (int i = 0; i < S / 2; ++i) {
+        const float2 e = __fmul2_rn(dt2, make_float2(A2[2 * i], A2[2 * i + 1]));
+        const float2 c2 = *reinterpret_cast<const float2*>(&tl.c[k][2 * i]);
+        const float2 mm = __fmul2_rn(make_float2(ex2(e.x), ex2(e.y)),
+                                     __ffma2_rn(c2, gy2, make_float2(m[2 * i], m[2 * i + 1])));
+        m[2 * i] = mm.x;
+        m[2 * i + 1] = mm.y;
+      }
       tsum += dt;
     }
     kahan_add(Ssum, Scomp, tsum);
   }
   if (!valid) return;
-  const int64_t ci = ((int64_t)(chunk - 1) * p.batch + b) * Dm + d;
+  const int64_t ci = ((int64_t)(sub - p.rsub) * p.batch + b) * Dm + d;
 #pragma unroll
   for (int n = 0; n < S; ++n)
     if (n < N) p.ws_M[ci * N + n] = m[n];
@@ -249,8 +259,8 @@ __global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
   float kap[S];
 #pragma unroll
   for (int n = 0; n < S; ++n) kap[n] = (p.dfinal && n < N) ? p.dfinal[sidx + n] : 0.f;
-  for (int cc = p.nchunks - 1; cc > chunk; --cc) {
-    const int64_t ci = ((int64_t)(cc - 1) * p.batch + b) * Dm + dd;
+  for (int sc = p.nchunks * p.rsub - 1; sc >= (chunk + 1) * p.rsub; --sc) {
+    const int64_t ci = ((int64_t)(sc - p.rsub) * p.batch + b) * Dm + dd;
     const float Sc = p.ws_S2[ci];
 #pragma unroll
     for (int n = 0; n < S; ++n)

@@ -28,13 +28,15 @@ struct BwdParams {
   float* dh_init;        // nullable
   const float* ws_H;     // forward chunk aggregates (end states), chunks 0 .. nchunks-2
   const float* ws_S;     // forward chunk step sums
-  float* ws_M;           // reverse chunk aggregates, chunks 1 .. nchunks-1
+  float* ws_M;           // reverse aggregates of the sub-chunks of chunks 1 .. nchunks-1
   float* ws_S2;          // their step sums
   float* ws_ck;          // state checkpoints, (ceil(L / seg), batch, dim, S)
   int64_t batch, seqlen, dim;
   int dstate;
   int nchunks;
   int64_t chunk_len;
+  int rsub;              // sub-chunks per chunk of the reverse aggregate pass
+  int64_t rsub_len;      // chunk_len / rsub
   int delta_softplus;
 };
 

@@ -581,10 +581,18 @@ int scan_backward(const void* x, const void* delta, const float* A, const void* 
   len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
   const int nchunks = (int)((d.seqlen + len - 1) / len);
 
+  // the reverse aggregate pass runs rsub sub-chunks per chunk (at most 4, a power of
+  // two, so that sub-chunks stay multiples of 8 steps) to reach ~24 warps per SM
+  int rsub = 1;
+  if (nchunks > 1) {
+    const int64_t warps = (int64_t)(nchunks - 1) * d.batch * gx;
+    while (rsub < 4 && warps * rsub * 2 <= (int64_t)sms * 24) rsub *= 2;
+  }
   const size_t nH = (size_t)(nchunks - 1) * d.batch * d.dim * d.dstate;
   const size_t nS = (size_t)(nchunks - 1) * d.batch * d.dim;
+  const size_t nM = nH * rsub, nS2 = nS * rsub;
   const size_t nck = (size_t)((d.seqlen + bk.seg - 1) / bk.seg) * d.batch * d.dim * S;
-  const size_t bytes = (2 * nH + 2 * nS + nck) * sizeof(float);
+  const size_t bytes = (nH + nS + nM + nS2 + nck) * sizeof(float);
   cudaMemPool_t pool;
   if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
   void* ws = nullptr;
@@ -597,10 +605,11 @@ int scan_backward(const void* x, const void* delta, const float* A, const void* 
   bp.bias = delta_bias; bp.h_init = h_init; bp.dout = dout; bp.dfinal = dfinal;
   bp.dx = dx; bp.ddelta = ddelta; bp.dz = dz; bp.dA = dA; bp.dB = dB; bp.dC = dC; bp.dD = dD;
   bp.dbias = ddelta_bias; bp.dh_init = dh_init;
-  bp.ws_H = w0; bp.ws_S = w0 + nH; bp.ws_M = w0 + nH + nS; bp.ws_S2 = w0 + 2 * nH + nS;
-  bp.ws_ck = w0 + 2 * nH + 2 * nS;
+  bp.ws_H = w0; bp.ws_S = w0 + nH; bp.ws_M = w0 + nH + nS; bp.ws_S2 = w0 + nH + nS + nM;
+  bp.ws_ck = w0 + nH + nS + nM + nS2;
   bp.batch = d.batch; bp.seqlen = d.seqlen; bp.dim = d.dim; bp.dstate = (int)d.dstate;
   bp.nchunks = nchunks; bp.chunk_len = len; bp.delta_softplus = d.delta_softplus;
+  bp.rsub = rsub; bp.rsub_len = len / rsub;
 
   int rc = SSM_OK;
   if (nchunks > 1) {
@@ -631,8 +640,8 @@ int scan_backward(const void* x, const void* delta, const float* A, const void* 
       rc = launch(agg, 0, dim3((unsigned)((d.dim + agg.ch - 1) / agg.ch), (unsigned)(nchunks - 1),
                                (unsigned)d.batch), maps, p, stream);
     if (rc == SSM_OK)
-      rc = launch_bwd(bk.reverse_aggregate, 3, dim3(gx, (unsigned)(nchunks - 1), (unsigned)d.batch), bp,
-                      stream);
+      rc = launch_bwd(bk.reverse_aggregate, 3, dim3(gx, (unsigned)((nchunks - 1) * rsub), (unsigned)d.batch),
+                      bp, stream);
   }
   if (rc == SSM_OK) rc = launch_bwd(bk.main, 4, dim3(gx, (unsigned)nchunks, (unsigned)d.batch), bp, stream);
   if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
