@@ -168,8 +168,8 @@ int ssm_conv_selective_scan_fwd(const void* x, const float* conv_w, const float*
  * No output may overlap an input or another output.  Sums over channels are
  * accumulated with fp32 atomic additions, so their rounding order is not fixed.
  * Other forms return SSM_ERR_UNSUPPORTED.  Long sequences are chunked; the
- * workspace (chunk carries and a state checkpoint every 8 steps:
- * ceil(seqlen / 8) * batch * dim * padded dstate fp32) comes from the library's
+ * workspace (chunk carries and a state checkpoint every 4 steps:
+ * ceil(seqlen / 4) * batch * dim * padded dstate fp32) comes from the library's
  * stream-ordered pool.
  */
 int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A,

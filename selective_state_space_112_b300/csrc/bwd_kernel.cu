@@ -30,7 +30,7 @@ namespace ssm {
 
 namespace {
 
-constexpr int SEG = 8;  // steps per tile and per rebuilt segment (chunks are multiples of 32)
+constexpr int SEG = 4;  // steps per tile and per rebuilt segment (chunks are multiples of 32)
 
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
 
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
 }
 
 template <typename IO, int S>
-__global__ void __launch_bounds__(32) bwd_main(const BwdParams p) {
+__global__ void __launch_bounds__(32, 12) bwd_main(const BwdParams p) {
   __shared__ float2 hist[SEG + 1][S / 2][32];  // state pairs; row 0: state before the segment
   __shared__ float dts[SEG][32];
   __shared__ Tile<S> tl;

@@ -565,12 +565,16 @@ int scan_backward(const void* x, const void* delta, const float* A, const void* 
     return SSM_ERR_CUDA;
   if (d.batch > 65535) return SSM_ERR_DIMS;
 
-  // chunks: one warp per 32 channels and chunk; as many chunks as give 8 warps per SM
-  // (chunks of at least min_chunk_len steps)
+  // chunks: one warp per 32 channels and chunk; as many chunks as fill every SM with
+  // the main kernel's resident CTAs in one wave (chunks of at least min_chunk_len steps)
   const unsigned gx = (unsigned)((d.dim + 31) / 32);
   int64_t k = g_opt_chunks.load();
   if (k <= 0) {
-    const int64_t warps = d.batch * gx, want = (int64_t)sms * 8;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)bk.main, 32, 0) != cudaSuccess ||
+        occ < 1)
+      occ = 8;
+    const int64_t warps = d.batch * gx, want = (int64_t)sms * occ;
     k = warps >= want ? 1 : std::max<int64_t>(1, want / warps);
     k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / std::max<int64_t>(ssm::kChunkAlign,
                                                                                  g_opt_min_chunk_len.load())));
