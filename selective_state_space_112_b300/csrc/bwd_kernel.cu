@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(32) bwd_reverse_aggregate(const BwdParams p) {
 }
 
 template <typename IO, int S>
-__global__ void __launch_bounds__(32, 12) bwd_main(const BwdParams p) {
+__global__ void __launch_bounds__(32, 16) bwd_main(const BwdParams p) {
   __shared__ float2 hist[SEG + 1][S / 2][32];  // state pairs; row 0: state before the segment
   __shared__ float dts[SEG][32];
   __shared__ Tile<S> tl;

@@ -585,12 +585,13 @@ int scan_backward(const void* x, const void* delta, const float* A, const void* 
   len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
   const int nchunks = (int)((d.seqlen + len - 1) / len);
 
-  // the reverse aggregate pass runs rsub sub-chunks per chunk (at most 4, a power of
-  // two, so that sub-chunks stay multiples of 8 steps) to reach ~24 warps per SM
+  // the reverse aggregate pass (a light kernel, 32 resident CTAs per SM) runs rsub
+  // sub-chunks per chunk (at most 4, a power of two, so that sub-chunks stay multiples
+  // of 8 steps) to come near 32 warps per SM
   int rsub = 1;
   if (nchunks > 1) {
     const int64_t warps = (int64_t)(nchunks - 1) * d.batch * gx;
-    while (rsub < 4 && warps * rsub * 2 <= (int64_t)sms * 24) rsub *= 2;
+    while (rsub < 4 && warps * rsub * 2 <= (int64_t)sms * 32) rsub *= 2;
   }
   const size_t nH = (size_t)(nchunks - 1) * d.batch * d.dim * d.dstate;
   const size_t nS = (size_t)(nchunks - 1) * d.batch * d.dim;
