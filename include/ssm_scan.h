@@ -130,9 +130,9 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
  *                or zero-fills it without state_in).  It must not overlap any
  *                other tensor.
  * All other arguments as ssm_selective_scan_fwd.  Built for time-varying B and C
- * (SSM_BC_TIME_VARYING), bbar_mode 0 and dstate <= 16; other forms return
- * SSM_ERR_UNSUPPORTED.  A long sequence run in pieces with state_in and both
- * states carried gives the result of one call over the whole sequence.
+ * (SSM_BC_TIME_VARYING) and bbar_mode 0; other forms return SSM_ERR_UNSUPPORTED.
+ * A long sequence run in pieces with state_in and both states carried gives the
+ * result of one call over the whole sequence.
  */
 int ssm_conv_selective_scan_fwd(const void* x, const float* conv_w, const float* conv_b,
                                 float* conv_state, const void* delta, const float* A,

@@ -38,11 +38,8 @@ KernelInfo kernel_info() {
 
 template <typename IO, bool LTI, int PASS, int VAR>
 KernelInfo pick_sg(int S, int G) {
-  // the prologue form (VAR 2) is built for one lane per channel only
-#define SSM_CASE(s_, g_)                                        \
-  if constexpr (VAR != 2 || g_ == 1) {                          \
-    if (S == s_ && G == g_) return kernel_info<IO, s_, g_, LTI, PASS, VAR>(); \
-  }
+#define SSM_CASE(s_, g_) \
+  if (S == s_ && G == g_) return kernel_info<IO, s_, g_, LTI, PASS, VAR>();
   SSM_FOR_EACH_SG(SSM_CASE)
 #undef SSM_CASE
   return KernelInfo();

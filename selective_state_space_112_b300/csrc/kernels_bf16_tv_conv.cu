@@ -1,4 +1,4 @@
-// Instantiations of the tiled selective-scan kernel: bf16 inputs, time-varying B and C, the Mamba-block prologue (causal conv of width 4 + silu on x), one lane per channel.
+// Instantiations of the tiled selective-scan kernel: bf16 inputs, time-varying B and C, the Mamba-block prologue (causal conv of width 4 + silu on x).
 #include "kernel_table.cuh"
 
 namespace ssm {

@@ -492,9 +492,9 @@ __device__ __forceinline__ float reduce_scatter(const float (&v)[G], int g) {
 //         0 .. nchunks-2.
 // PASS 1: output pass (carry-in, out, final state).
 // VAR 0: the scan as stated; VAR 1: exact zero-order-hold input term (bbar_mode 1);
-// VAR 2: the Mamba-block prologue (depthwise causal conv of width 4 + silu on x),
-// one lane per channel.  Separate instantiations, so that the common path carries
-// none of the other forms' registers.
+// VAR 2: the Mamba-block prologue (depthwise causal conv of width 4 + silu on x).
+// Separate instantiations, so that the common path carries none of the other forms'
+// registers.
 template <typename IO, int S, int G, bool LTI, int PASS, int VAR>
 __global__ void __launch_bounds__(Geo<IO, S, G>::NT)
 scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
@@ -504,7 +504,6 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
   constexpr bool OUT = (PASS == 1);
   constexpr bool MFORM = LTI || !IO::kFastDecay;
   constexpr bool ZOH = (VAR == 1), CONV = (VAR == 2);
-  static_assert(!CONV || G == 1, "the prologue runs one lane per channel");
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::OFF_BAR);  // raw tile landed (TMA)
   uint64_t* ready = full + ST;                                         // fp32 B / C planes written
@@ -793,8 +792,9 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
     for (int i = 0; i < S / 2; ++i) h[i] = f2(hv[2 * i], hv[2 * i + 1]);
   }
 
-  // block prologue: taps, bias and the window of the three raw inputs before the
-  // next step (xw0 oldest); a chunk after the first starts from the inputs before it
+  // block prologue: taps, bias and the window of the channel's three raw inputs
+  // before the next group of rounds (xw0 oldest), held by every lane of the channel; a
+  // chunk after the first starts from the inputs before it
   [[maybe_unused]] float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
   [[maybe_unused]] float cbv = 0.f, xw0 = 0.f, xw1 = 0.f, xw2 = 0.f;
   if constexpr (CONV) {
@@ -811,7 +811,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
       xw0 = src[ci3];
       xw1 = src[ci3 + 1];
       xw2 = src[ci3 + 2];
-      if (PASS == 0 && p.ws_cs && valid) {
+      if (PASS == 0 && p.ws_cs && valid && g == 0) {
         p.ws_cs[ci3] = xw0;
         p.ws_cs[ci3 + 1] = xw1;
         p.ws_cs[ci3 + 2] = xw2;
@@ -858,20 +858,33 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
         }
         if constexpr (CONV) {
           // u_t = silu(w0 x_t + w1 x_{t-1} + w2 x_{t-2} + w3 x_{t-3} + b): the scan and
-          // the D skip take u; the window keeps the group's last three raw inputs
-          float ext[R + 3];
+          // the D skip take u.  Every lane of the channel gathers the group's G R raw
+          // inputs (lane j holds step G q + j) and the window; each lane evaluates the
+          // convolution at the G positions of a round and keeps its own.
+          float ext[G * R + 3];
           ext[0] = xw0;
           ext[1] = xw1;
           ext[2] = xw2;
 #pragma unroll
-          for (int q = 0; q < R; ++q) ext[q + 3] = xv[q];
-          xw0 = ext[R];
-          xw1 = ext[R + 1];
-          xw2 = ext[R + 2];
-#pragma unroll
           for (int q = 0; q < R; ++q)
-            xv[q] = silu(fmaf(cw.x, ext[q + 3], fmaf(cw.y, ext[q + 2], fmaf(cw.z, ext[q + 1],
-                                                                            fmaf(cw.w, ext[q], cbv)))));
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+              ext[3 + G * q + j] = (G == 1) ? xv[q] : __shfl_sync(0xffffffffu, xv[q], gbase + j);
+          xw0 = ext[G * R];
+          xw1 = ext[G * R + 1];
+          xw2 = ext[G * R + 2];
+#pragma unroll
+          for (int q = 0; q < R; ++q) {
+            float pre = 0.f;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              const int e = 3 + G * q + j;  // step G q + j of the group
+              const float pj = fmaf(cw.x, ext[e], fmaf(cw.y, ext[e - 1], fmaf(cw.z, ext[e - 2],
+                                                                              fmaf(cw.w, ext[e - 3], cbv))));
+              pre = (G == 1 || j == g) ? pj : pre;
+            }
+            xv[q] = silu(pre);
+          }
         }
         if (p.delta_softplus) {
           // rows past the sequence end hold delta = -inf: step 0, an identity step
@@ -954,7 +967,7 @@ scan_tile_kernel(const __grid_constant__ TmaMaps maps, const ScanParams p) {
 
   // ---- results
   if (PASS == 1) {
-    if (CONV && chunk == p.nchunks - 1 && p.conv_state_out && valid) {
+    if (CONV && chunk == p.nchunks - 1 && p.conv_state_out && valid && g == 0) {
       // the last three raw inputs of the history-extended sequence, oldest first (a
       // sequence shorter than three keeps part of the history; then there is one
       // chunk, and this lane read that history itself)

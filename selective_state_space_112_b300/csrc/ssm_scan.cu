@@ -354,10 +354,8 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     const void* cptrs[] = {conv->w, conv->b, conv->state};
     for (const void* q : cptrs)
       if (q && ((uintptr_t)q & 15u)) return SSM_ERR_ALIGN;
-    // the prologue form: time-varying B and C, the fused scan's input term, one lane
-    // per channel (N <= 16)
-    if (d.bc_layout != SSM_BC_TIME_VARYING || d.bbar_mode != 0 || d.dstate > 16)
-      return SSM_ERR_UNSUPPORTED;
+    // the prologue form: time-varying B and C and the fused scan's input term
+    if (d.bc_layout != SSM_BC_TIME_VARYING || d.bbar_mode != 0) return SSM_ERR_UNSUPPORTED;
   }
   float* const cstate = conv ? conv->state : nullptr;
   const float* const chist = (conv && d.state_in) ? conv->state : nullptr;

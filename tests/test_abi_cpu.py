@@ -109,8 +109,8 @@ def call_conv(d, **over):
 def test_conv_entry_host_checks():
     """The block-prologue entry checks its own arguments on the host: taps are
     required, every pointer 16-byte aligned, the history disjoint from the other
-    tensors; the forms it is not built for (constant B and C, the exact-ZOH term,
-    N > 16) are SSM_ERR_UNSUPPORTED before anything touches the device."""
+    tensors; the forms it is not built for (constant B and C, the exact-ZOH term)
+    are SSM_ERR_UNSUPPORTED before anything touches the device."""
     assert call_conv(dims(), cw=0) == -1
     for k in ("cw", "cb", "cs"):
         assert call_conv(dims(), **{k: CP[k] + 4}) == -3, k
@@ -118,7 +118,17 @@ def test_conv_entry_host_checks():
     assert call_conv(dims(), cs=P["fs"]) == -6
     assert call_conv(dims(bc_layout=1)) == -4
     assert call_conv(dims(bbar_mode=1)) == -4
-    assert call_conv(dims(dstate=32)) == -4
+    assert call_conv(dims(dstate=65)) == -2
+
+
+def test_conv_entry_accepts_wide_states_on_the_host():
+    """N up to 64 (two and four lanes per channel) passes the prologue entry's host
+    validation: without a GPU the call fails only at the device (SSM_ERR_CUDA)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for n in (24, 32, 64):
+        assert call_conv(dims(dstate=n)) == -5, n
 
 
 def test_no_cpu_fallback():

@@ -82,6 +82,42 @@ def test_conv_prologue_parity(name, kw, ckw, chunks, tma, io):
         ssm.ssm_set_option("tma", 1)
 
 
+LANE_CASES = [
+    # (name, workload kwargs, conv kwargs, forced chunks, tma, lanes per channel)
+    ("g2_ragged_D", dict(batch=2, seqlen=300, dim=136, dstate=16), {}, 0, 1, 2),
+    ("g2_chunks5_hist", dict(batch=2, seqlen=700, dim=96, dstate=16, state_in=True),
+     dict(hist=True), 5, 1, 2),
+    ("g2_chunks3_generic", dict(batch=2, seqlen=400, dim=72, dstate=16, state_in=True),
+     dict(hist=True), 3, 0, 2),
+    ("g4_ragged_L", dict(batch=3, seqlen=77, dim=64, dstate=16), {}, 2, 1, 4),
+    ("g4_N13", dict(batch=2, seqlen=96, dim=64, dstate=13), {}, 0, 1, 4),
+    ("g2_N32_hist", dict(batch=2, seqlen=260, dim=80, dstate=32, state_in=True), dict(hist=True), 3, 1, 2),
+    ("g4_N64", dict(batch=2, seqlen=140, dim=48, dstate=64), {}, 2, 1, 4),
+    ("g4_N24_generic", dict(batch=2, seqlen=150, dim=40, dstate=24, gate=False, with_bias=False),
+     dict(with_bias=False), 0, 0, 4),
+]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("name,kw,ckw,chunks,tma,lanes", LANE_CASES, ids=[c[0] for c in LANE_CASES])
+def test_conv_prologue_lanes_per_channel(name, kw, ckw, chunks, tma, lanes, io):
+    """Two and four lanes per channel (each lane gathers its channel's raw inputs of
+    a group of rounds by shuffles and keeps the convolution at its own steps), and
+    states past 16 (N 24, 32, 64), which only those layouts cover."""
+    import selective_state_space_112_b300 as ssm
+    w = make_workload(name, io=io, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    cv = make_conv(w, **ckw)
+    try:
+        ssm.ssm_set_option("chunks", chunks)
+        ssm.ssm_set_option("tma", tma)
+        ssm.ssm_set_option("lanes", lanes)
+        check(w, cv, f"{name}/{io}")
+    finally:
+        ssm.ssm_set_option("chunks", 0)
+        ssm.ssm_set_option("tma", 1)
+        ssm.ssm_set_option("lanes", 0)
+
+
 def test_conv_prologue_without_softplus_ragged():
     """Steps past the sequence end without softplus take the per-step test path.
     The steps are given directly (small positive values, no bias)."""
