@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for the Mamba (S6) selective-scan forward pass.
+"""Float64 CPU oracle for the Mamba (S6) selective scan and the Mamba-2 SSD layer.
 
 TEST INFRASTRUCTURE ONLY.  This package is the slow, obviously correct
 reference that the CUDA kernels are checked against.  Only ``tests/``,
@@ -11,9 +11,10 @@ only loads that library, widens the stored input values (fp32, or bf16 given
 as its raw 16-bit patterns) exactly to float64, and slices inputs.
 
 Sources: the pages "State-space models" (rayaq.ca; sections Discretization,
-Recurrence and convolution, Mamba: selection, Implementation) and
-"Structured State Space Models and Mamba" (llms.blog; sections Discretization
-Mechanics, the S6 section, Hardware-Aware Parallel Associative Scan).
+Recurrence and convolution, Mamba: selection, The parallel scan, Implementation)
+and "Structured State Space Models and Mamba" (llms.blog; sections Discretization
+Mechanics, the S6 section, Hardware-Aware Parallel Associative Scan, State Space
+Duality and Mamba-2).
 
 Every function here is pinned in ``tests/test_oracle_pins.py``.
 """
@@ -73,6 +74,8 @@ def _load():
             lib.oracle_conv_silu.argtypes = [pd] * 6 + [i64] * 4 + [i32]
             lib.oracle_selective_scan_bwd_f64.restype = i32
             lib.oracle_selective_scan_bwd_f64.argtypes = [pd] * 20 + [i64] * 4 + [i32] * 2
+            lib.oracle_ssd_f64.restype = i32
+            lib.oracle_ssd_f64.argtypes = [pd] * 10 + [i64] * 6 + [i32] * 3
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -301,3 +304,34 @@ def causal_conv(x, K, D=None, io_dtype: str = "f32", threads: int = 0):
     if rc != 0:
         raise ValueError("oracle_causal_conv rejected its arguments")
     return out
+
+
+def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None, *, dt_softplus: bool = True,
+        io_dtype: str = "bf16", threads: int = 0):
+    """Mamba-2 SSD layer (scalar decay per head) stepped as a recurrence, float64.
+
+    Shapes: x, z: (batch, L, H, P); dt: (batch, L, H); A, D, dt_bias: (H,);
+    B, C: (batch, L, G, N) with head h reading group h // (H // G);
+    h0: (batch, H, P, N).  x, dt, z, B, C are stored as ``io_dtype``; A, D,
+    dt_bias and h0 are fp32/fp64 values.  Returns (out, final_state).
+    """
+    x64, dt64, z64 = widen(x, io_dtype), widen(dt, io_dtype), widen(z, io_dtype)
+    B64, C64 = widen(B, io_dtype), widen(C, io_dtype)
+    A64, D64, bias64 = widen(A), widen(D), widen(dt_bias)
+    batch, L, H, P = x64.shape
+    G, N = B64.shape[2], B64.shape[3]
+    assert dt64.shape == (batch, L, H) and A64.shape == (H,)
+    assert B64.shape == (batch, L, G, N) and C64.shape == B64.shape
+    if z64 is not None:
+        assert z64.shape == x64.shape
+    state = (np.array(h0, dtype=np.float64, order="C", copy=True) if h0 is not None
+             else np.zeros((batch, H, P, N), dtype=np.float64))
+    assert state.shape == (batch, H, P, N)
+    out = np.empty_like(x64)
+    rc = _load().oracle_ssd_f64(
+        _ptr(x64), _ptr(dt64), _ptr(A64), _ptr(B64), _ptr(C64), _ptr(D64), _ptr(z64),
+        _ptr(bias64), _ptr(out), _ptr(state), batch, L, H, P, G, N, int(dt_softplus),
+        int(h0 is not None), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_ssd_f64 rejected its arguments")
+    return out, state

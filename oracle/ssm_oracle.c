@@ -1,5 +1,5 @@
 /*
- * Float64 CPU oracle for the Mamba (S6) selective-scan forward pass.
+ * Float64 CPU oracle for the Mamba (S6) selective scan and the Mamba-2 SSD layer.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
  * reference that the CUDA kernels are checked against.  Only the test suite,
@@ -399,6 +399,81 @@ int oracle_selective_scan_bwd_f64(
     free(vs);
   }
   return 0;
+}
+
+/*
+ * Mamba-2 state-space-duality (SSD) layer, forward, stepped as a recurrence
+ * ("State-space models", section "The parallel scan": Mamba-2 restricts A to a
+ * scalar times the identity per head; "State Space Models: Mamba and Beyond",
+ * section "Beyond Mamba: state-space duality and hybrid architectures": A is a
+ * scalar per attention-style head; "Structured State Space Models and Mamba",
+ * section "State Space Duality and Mamba-2": the same map written as masked
+ * attention Y = (L o (C B^T)) V, which the tests use as a pin).
+ *
+ * Shapes: x, z, out: (batch, L, H, P); dt: (batch, L, H); A, D, dt_bias: (H);
+ * B, C: (batch, L, G, N), head h reading group h / (H / G); state:
+ * (batch, H, P, N), read as h_{-1} when state_in, else h_{-1} = 0; written with
+ * h_{L-1} when not NULL.  For each batch row b, head h, step t:
+ *   s      = dt[b,t,h] + dt_bias[h];  step = softplus(s) if dt_softplus else s
+ *   a      = exp(step * A[h])                      one decay for the whole head
+ *   h[p,n] = a * h[p,n] + step * B[b,t,g,n] * x[b,t,h,p]
+ *   y[p]   = sum_n C[b,t,g,n] h[p,n] + D[h] x[b,t,h,p]
+ *   out    = y * silu(z[b,t,h,p])  (or y without a gate)
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_ssd_f64(const double* x, const double* dt, const double* A,
+                   const double* B, const double* C, const double* D,
+                   const double* z, const double* dt_bias, double* out,
+                   double* state, int64_t batch, int64_t seqlen, int64_t nheads,
+                   int64_t headdim, int64_t ngroups, int64_t dstate,
+                   int dt_softplus, int state_in, int nthreads) {
+  if (batch < 0 || seqlen < 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 ||
+      dstate <= 0 || nheads % ngroups != 0)
+    return -1;
+  if (state_in && state == NULL) return -1;
+  const int64_t per_group = nheads / ngroups;
+  const int64_t P = headdim, N = dstate, H = nheads;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < batch * H; ++bh) {
+    const int64_t b = bh / H, h = bh % H, g = h / per_group;
+    double* hs = (double*)malloc((size_t)(P * N) * sizeof(double));
+    if (!hs) {
+#pragma omp atomic write
+      bad = 1;
+      continue;
+    }
+    for (int64_t i = 0; i < P * N; ++i)
+      hs[i] = state_in ? state[(b * H + h) * P * N + i] : 0.0;
+    for (int64_t t = 0; t < seqlen; ++t) {
+      const double s = dt[(b * seqlen + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+      const double step = dt_softplus ? oracle_softplus(s) : s;
+      const double a = exp(step * A[h]);
+      const double* Bv = &B[((b * seqlen + t) * ngroups + g) * N];
+      const double* Cv = &C[((b * seqlen + t) * ngroups + g) * N];
+      const int64_t row = ((b * seqlen + t) * H + h) * P;
+      for (int64_t p = 0; p < P; ++p) {
+        const double xv = x[row + p];
+        double y = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;
+          y += Cv[n] * hs[p * N + n];
+        }
+        y += (D ? D[h] : 0.0) * xv;
+        if (z) y *= silu(z[row + p]);
+        out[row + p] = y;
+      }
+    }
+    if (state)
+      for (int64_t i = 0; i < P * N; ++i) state[(b * H + h) * P * N + i] = hs[i];
+    free(hs);
+  }
+  return bad ? -1 : 0;
 }
 
 /* Number of threads OpenMP would use (1 without OpenMP). */

@@ -19,7 +19,16 @@ Block prologue (``make_conv``, its own generator seeded with seed + 7919):
   conv bias    ~ U[-1/2, 1/2] per channel
   history      ~ N(0, 1) per (b, d, 3), the inputs before the sequence
 Draw order: x, delta_raw, dt, A, B, C, D, z, h_init, from numpy's PCG64 seeded
-with the workload's seed.  bf16 inputs are the fp32 draws rounded to nearest
+with the workload's seed.
+Mamba-2 SSD layer (``make_ssd``; the same distributions with the decay, the step
+and D per head):
+  x, z         ~ N(0, 1)                      (batch, L, H, P)
+  dt_raw       ~ N(0, 1)                      (batch, L, H)
+  dt_h         ~ U[0.001, 0.1] per head;  dt_bias = log(expm1(dt_h))
+  A            = -exp(N(0, variance 0.5)) per head
+  B, C         ~ N(0, 1) per (b, t, group, n)
+  D            ~ N(0, 1) per head;  h_init ~ N(0, 1) per (b, h, p, n)
+  draw order x, dt_raw, dt, A, B, C, D, z, h_init.  bf16 inputs are the fp32 draws rounded to nearest
 even bfloat16 and are carried as raw uint16 bit patterns; A, D, delta_bias and
 h_init stay fp32.
 """
@@ -189,3 +198,65 @@ def make_conv(w: Workload, *, with_bias: bool = True, hist: bool = False, width:
 
 def config(name: str) -> Workload:
     return make_workload(name, **CONFIGS[name])
+
+
+@dataclass
+class SsdWorkload:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    io: str
+    x: np.ndarray                 # (batch, L, H, P)
+    dt: np.ndarray                # (batch, L, H), raw step before bias and softplus
+    A: np.ndarray                 # (H,) fp32, one decay rate per head
+    B: np.ndarray                 # (batch, L, G, N)
+    C: np.ndarray                 # (batch, L, G, N)
+    D: Optional[np.ndarray]       # (H,) fp32
+    z: Optional[np.ndarray]       # (batch, L, H, P)
+    dt_bias: Optional[np.ndarray]  # (H,) fp32
+    h0: Optional[np.ndarray]      # (batch, H, P, N) fp32
+    dt_softplus: bool = True
+    seed: int = 0
+
+    @property
+    def tokens_channels(self) -> int:
+        return self.batch * self.seqlen * self.nheads * self.headdim
+
+
+def make_ssd(name: str, batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, *,
+             ngroups: int = 1, io: str = "bf16", seed: int = 0, gate: bool = True,
+             state_in: bool = False, with_D: bool = True, with_bias: bool = True) -> SsdWorkload:
+    """Draw one Mamba-2 SSD workload following the module recipe."""
+    assert io == "bf16" and nheads % ngroups == 0
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shp = (batch, seqlen, nheads, headdim)
+    x = rng.standard_normal(shp, dtype=np.float32)
+    dt_raw = rng.standard_normal((batch, seqlen, nheads), dtype=np.float32)
+    dt = rng.uniform(0.001, 0.1, size=nheads)
+    A = (-np.exp(rng.normal(0.0, np.sqrt(0.5), size=nheads))).astype(np.float32)
+    B = rng.standard_normal((batch, seqlen, ngroups, dstate), dtype=np.float32)
+    C = rng.standard_normal((batch, seqlen, ngroups, dstate), dtype=np.float32)
+    D = rng.standard_normal(nheads, dtype=np.float32) if with_D else None
+    z = rng.standard_normal(shp, dtype=np.float32) if gate else None
+    h0 = (rng.standard_normal((batch, nheads, headdim, dstate), dtype=np.float32)
+          if state_in else None)
+    bias = np.log(np.expm1(dt)).astype(np.float32) if with_bias else None
+    return SsdWorkload(name=name, batch=batch, seqlen=seqlen, nheads=nheads, headdim=headdim,
+                       ngroups=ngroups, dstate=dstate, io=io, x=f32_to_bf16_bits(x),
+                       dt=f32_to_bf16_bits(dt_raw), A=A, B=f32_to_bf16_bits(B),
+                       C=f32_to_bf16_bits(C), D=D,
+                       z=None if z is None else f32_to_bf16_bits(z), dt_bias=bias, h0=h0,
+                       seed=seed)
+
+
+# Mamba-2-shaped SSD layers: 2.7B-like (d_inner 5120 = 80 heads of 64, N 128, one
+# group) and the same width with N 256 (the state size the pages give for Mamba-2).
+SSD_CONFIGS = {
+    "ssd_tiny": dict(batch=1, seqlen=200, nheads=4, headdim=64, dstate=64, seed=20),
+    "mamba2_2p7b_bf16": dict(batch=4, seqlen=4096, nheads=80, headdim=64, dstate=128, seed=21),
+    "mamba2_n256_bf16": dict(batch=4, seqlen=4096, nheads=80, headdim=64, dstate=256, seed=22),
+}

@@ -49,6 +49,16 @@ MUTANTS = {
     "bwd_dx_no_skip": ("dx[i] = gx + gy * (D ? D[d] : 0.0);", "dx[i] = gx;"),
     "bwd_dA_no_step": ("dA[d * N + n] += lam * hprev * a * dts[t];", "dA[d * N + n] += lam * hprev * a;"),
     "bwd_dz_plain_sigmoid": ("dz[i] = dout[i] * y * sz * (1.0 + z[i] * (1.0 - sz));", "dz[i] = dout[i] * y * sz;"),
+    "ssd_group_modulo": ("const int64_t b = bh / H, h = bh % H, g = h / per_group;",
+                         "const int64_t b = bh / H, h = bh % H, g = h % ngroups;"),
+    "ssd_decay_positive": ("const double a = exp(step * A[h]);", "const double a = exp(-step * A[h]);"),
+    "ssd_input_no_step": ("hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;",
+                          "hs[p * N + n] = a * hs[p * N + n] + Bv[n] * xv;"),
+    "ssd_readout_before_update": ("          hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;\n          y += Cv[n] * hs[p * N + n];",
+                                  "          y += Cv[n] * hs[p * N + n];\n          hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;"),
+    "ssd_skip_dropped": ("y += (D ? D[h] : 0.0) * xv;", "y += 0.0 * xv;"),
+    "ssd_state_transposed": ("hs[i] = state_in ? state[(b * H + h) * P * N + i] : 0.0;",
+                             "hs[i] = state_in ? state[(b * H + h) * P * N + (i % N) * P + i / N] : 0.0;"),
     "bwd_dh0_undecayed": ("dh0[(b * dim + d) * N + n] = a_next[n] * lam_next[n];",
                           "dh0[(b * dim + d) * N + n] = lam_next[n];"),
 }

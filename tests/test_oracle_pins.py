@@ -546,3 +546,123 @@ def test_backward_matches_autograd_of_an_independent_forward():
     for arg, gname in [("x", "dx"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"),
                        ("D", "dD"), ("z", "dz"), ("delta_bias", "dbias"), ("h0", "dh0")]:
         np.testing.assert_allclose(g[gname], T[arg].grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=gname)
+
+
+# ------------------------------------------------ Mamba-2 SSD (scalar decay per head)
+
+def _ssd_case(seed, *, batch=2, L=23, H=4, P=3, G=2, N=5, state_in=True, gate=True):
+    from selective_state_space_112_b300.workloads import make_ssd
+    return make_ssd("pin", batch, L, H, P, N, ngroups=G, seed=seed, gate=gate, state_in=state_in)
+
+
+def _ssd_inputs64(w):
+    wd = lambda a: None if a is None else oracle.widen(a, "bf16")
+    f = lambda a: None if a is None else np.asarray(a, dtype=np.float64)
+    return (wd(w.x), wd(w.dt), f(w.A), wd(w.B), wd(w.C), f(w.D), wd(w.z), f(w.dt_bias), f(w.h0))
+
+
+def _ssd(w, **kw):
+    return oracle.ssd(w.x, w.dt, w.A, w.B, w.C, D=w.D, z=w.z, dt_bias=w.dt_bias, h0=w.h0, **kw)
+
+
+def _masked_attention(w, zero_decay=False):
+    """'Structured State Space Models and Mamba', section 'State Space Duality and
+    Mamba-2': Y = (L o (Q K^T)) V with Q = C, K = B, V = step * x and the
+    1-semiseparable L[i, j] = exp(A (S_i - S_j)) for j <= i (S = cumulative step
+    sums), plus the initial state's decayed readout, D x and the gate; the final
+    state is the same sum read at the last step.  One dense matrix per (b, head)."""
+    x, dtr, A, B, C, D, z, bias, h0 = _ssd_inputs64(w)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    v = dtr + (0.0 if bias is None else bias)
+    step = np.logaddexp(0.0, v)                                   # softplus, (b, L, H)
+    out = np.empty_like(x)
+    fin = np.empty((batch, H, P, N))
+    for b in range(batch):
+        for h in range(H):
+            g = h // (H // G)
+            a = 0.0 if zero_decay else A[h]
+            S = np.cumsum(step[b, :, h])
+            Lm = np.tril(np.exp(a * (S[:, None] - S[None, :])))   # (L, L)
+            QK = C[b, :, g] @ B[b, :, g].T                        # (L, L)
+            V = step[b, :, h, None] * x[b, :, h]                  # (L, P)
+            y = (Lm * QK) @ V
+            st = np.zeros((P, N)) if h0 is None else h0[b, h]
+            y += np.exp(a * S)[:, None] * (C[b, :, g] @ st.T)     # decayed initial state
+            if D is not None:
+                y += D[h] * x[b, :, h]
+            if z is not None:
+                y *= z[b, :, h] / (1.0 + np.exp(-z[b, :, h]))
+            out[b, :, h] = y
+            wlast = np.exp(a * (S[-1] - S)) * step[b, :, h]       # (L,)
+            fin[b, h] = np.exp(a * S[-1]) * st + (x[b, :, h] * wlast[:, None]).T @ B[b, :, g]
+    return out, fin
+
+
+@pytest.mark.parametrize("seed,state_in,gate", [(31, True, True), (32, False, True), (33, True, False)])
+def test_ssd_equals_masked_attention_form(seed, state_in, gate):
+    """The recurrence and the pages' masked-attention form give the same outputs and
+    final state (two heads per group, so the head-to-group map is exercised)."""
+    w = _ssd_case(seed, state_in=state_in, gate=gate)
+    out, st = _ssd(w)
+    ref, ref_st = _masked_attention(w)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(st, ref_st, rtol=1e-11, atol=1e-12)
+
+
+def test_ssd_is_the_selective_scan_with_a_tied_decay():
+    """'State-space models', section 'The parallel scan': Mamba-2 is the selective
+    SSM with A a scalar times the identity per head.  Every channel p of head h is
+    a channel of the S6 scan with A[d, n] = A[h], its head's step and D, and its
+    group's B and C, so the already pinned S6 oracle must give the same numbers."""
+    w = _ssd_case(34, G=2, H=4, P=3, N=5)
+    out, st = _ssd(w)
+    x, dtr, A, B, C, D, z, bias, h0 = _ssd_inputs64(w)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    for g in range(G):
+        heads = [h for h in range(H) if h // (H // G) == g]
+        xs = x[:, :, heads].reshape(batch, L, -1)
+        ds = np.repeat(dtr[:, :, heads], P, axis=2)
+        A1 = np.repeat(A[heads], P)[:, None] * np.ones((1, N))
+        o1, s1 = oracle.selective_scan(
+            xs, ds, A1, B[:, :, g], C[:, :, g], D=np.repeat(D[heads], P),
+            z=z[:, :, heads].reshape(batch, L, -1), delta_bias=np.repeat(bias[heads], P),
+            h0=h0[:, heads].reshape(batch, -1, N))
+        np.testing.assert_allclose(out[:, :, heads].reshape(batch, L, -1), o1, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(st[:, heads].reshape(batch, -1, N), s1, rtol=1e-13, atol=1e-14)
+
+
+def test_ssd_zero_decay_is_causal_linear_attention():
+    """The rugvailabs.com page on state-space models and Mamba, its passage on
+    Mamba-2 and state space duality: linear attention without softmax is the SSM
+    with input-dependent B and C and an identity transition.  With A = 0
+    the output is sum_{s <= t} (C_t . B_s) step_s x_s plus D x, gated."""
+    w = _ssd_case(35, state_in=False)
+    w.A = np.zeros_like(w.A)
+    out, st = _ssd(w)
+    ref, ref_st = _masked_attention(w, zero_decay=True)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(st, ref_st, rtol=1e-11, atol=1e-12)
+
+
+def test_ssd_split_resume_and_state_layout():
+    """Two calls carrying the (b, H, P, N) state equal one call; the state of a
+    single step from zero is step * B[n] * x[p] at index [b, h, p, n]."""
+    w = _ssd_case(36, state_in=True, L=17)
+    out, st = _ssd(w)
+    from dataclasses import replace
+    w1 = replace(w, x=w.x[:, :9], dt=w.dt[:, :9], B=w.B[:, :9], C=w.C[:, :9], z=w.z[:, :9])
+    o1, s1 = _ssd(w1)
+    w2 = replace(w, x=w.x[:, 9:], dt=w.dt[:, 9:], B=w.B[:, 9:], C=w.C[:, 9:], z=w.z[:, 9:], h0=s1)
+    o2, s2 = _ssd(w2)
+    np.testing.assert_allclose(np.concatenate([o1, o2], axis=1), out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(s2, st, rtol=1e-12, atol=1e-13)
+    w0 = _ssd_case(37, state_in=False, L=1, G=1, H=2, P=3, N=4)
+    _, s = _ssd(w0)
+    x, dtr, A, B, C, D, z, bias, h0 = _ssd_inputs64(w0)
+    step = np.logaddexp(0.0, dtr[:, 0] + bias)                    # (b, H)
+    for b in range(2):
+        for h in range(2):
+            np.testing.assert_allclose(s[b, h], step[b, h] * np.outer(x[b, 0, h], B[b, 0, 0]),
+                                       rtol=1e-14)
