@@ -1,7 +1,7 @@
-"""B300-native (sm_103a) Mamba S6 selective-scan forward.
+"""B300-native (sm_103a) Mamba S6 selective scan and Mamba-2 SSD layer.
 
 The compute lives in the C-ABI library ``libssmscan.so`` built from ``csrc/``
-(declarations in ``include/ssm_scan.h``).  This package only marshals PyTorch
+(declarations in ``include/ssm_scan.h`` and ``include/ssm_ssd.h``).  This package only marshals PyTorch
 tensors (used for device memory and streams) into that ABI; it never computes
 any part of the scan itself and has no CPU fallback.
 """
@@ -9,13 +9,14 @@ from __future__ import annotations
 
 from . import _abi
 from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, SSM_OK,
-                   SSMError, SsmDims)
+                   SSMError, SsdDims, SsmDims)
 
 __all__ = ["ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_bwd",
            "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
-           "ssm_profile_enable", "ssm_profile_read", "SSMError", "SsmDims"]
+           "ssm_profile_enable", "ssm_profile_read", "ssm_ssd_fwd", "SSMError", "SsmDims",
+           "SsdDims"]
 
 
 def _torch():
@@ -189,6 +190,57 @@ def _scan(x, delta, A, B, C, D, z, delta_bias, out, final_state, conv, *, delta_
         what = "ssm_selective_scan_fwd_noalloc" if noalloc else "ssm_selective_scan_fwd"
     if rc != SSM_OK:
         raise SSMError(rc, what)
+    return out, final_state
+
+
+def ssm_ssd_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, out=None, final_state=None, *,
+                dt_softplus: bool = True, state_in: bool = False, return_final_state: bool = True,
+                stream=None):
+    """Mamba-2 SSD layer forward on the current CUDA device.
+
+    x, z: (batch, L, H, P) bfloat16; dt: (batch, L, H) bfloat16 (raw step);
+    A, D, dt_bias: (H,) float32 (D, dt_bias may be None); B, C: (batch, L, G, N)
+    bfloat16, head h reading group h // (H // G).  With ``state_in`` the initial
+    state is read from ``final_state`` (batch, H, P, N) float32, which is then
+    overwritten with the final state.  Returns ``(out, final_state)``.
+    """
+    torch = _torch()
+    if x.dim() != 4:
+        raise ValueError("x must be (batch, L, heads, headdim)")
+    batch, L, H, P = x.shape
+    if B.dim() != 4:
+        raise ValueError("B must be (batch, L, groups, dstate)")
+    G, N = B.shape[2], B.shape[3]
+    io = SSM_BF16 if x.dtype == torch.bfloat16 else SSM_F32
+    for name, t, dty, shp in (
+            ("dt", dt, x.dtype, (batch, L, H)), ("z", z, x.dtype, x.shape),
+            ("A", A, torch.float32, (H,)), ("D", D, torch.float32, (H,)),
+            ("dt_bias", dt_bias, torch.float32, (H,)),
+            ("B", B, x.dtype, (batch, L, G, N)), ("C", C, x.dtype, (batch, L, G, N))):
+        if t is None:
+            continue
+        if t.dtype != dty or tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{name}: expected {dty} {tuple(shp)}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and (state_in or return_final_state):
+        if state_in:
+            raise ValueError("state_in needs final_state holding the initial state")
+        final_state = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device)
+    dims = SsdDims(batch=batch, seqlen=L, nheads=H, headdim=P, ngroups=G, dstate=N, io_dtype=io,
+                   dt_softplus=int(bool(dt_softplus)), state_in=int(bool(state_in)), reserved=0)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = _abi.call_ssd(_addr(x), _addr(dt), _addr(A), _addr(B), _addr(C), _addr(D), _addr(z),
+                       _addr(dt_bias), _addr(out), _addr(final_state), dims, int(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_ssd_fwd")
     return out, final_state
 
 

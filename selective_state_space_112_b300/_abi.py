@@ -29,7 +29,9 @@ EXPORTS = ("ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selecti
            "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
            "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
-           "ssm_profile_enable", "ssm_profile_read")
+           "ssm_profile_enable", "ssm_profile_read",
+           # include/ssm_ssd.h
+           "ssm_ssd_fwd")
 
 
 class SsmDims(ctypes.Structure):
@@ -38,6 +40,15 @@ class SsmDims(ctypes.Structure):
                 ("io_dtype", ctypes.c_int32), ("bc_layout", ctypes.c_int32),
                 ("delta_softplus", ctypes.c_int32), ("state_in", ctypes.c_int32),
                 ("bbar_mode", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SsdDims(ctypes.Structure):
+    """ssm_ssd_dims of include/ssm_ssd.h."""
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("dt_softplus", ctypes.c_int32),
+                ("state_in", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class SSMError(RuntimeError):
@@ -72,6 +83,8 @@ def lib():
             L.ssm_selective_scan_bwd.argtypes = [vp] * 20 + [ctypes.POINTER(SsmDims), vp]
             L.ssm_selective_scan_fwd_noalloc.restype = i32
             L.ssm_selective_scan_fwd_noalloc.argtypes = [vp] * 10 + [ctypes.POINTER(SsmDims), vp]
+            L.ssm_ssd_fwd.restype = i32
+            L.ssm_ssd_fwd.argtypes = [vp] * 10 + [ctypes.POINTER(SsdDims), vp]
             L.ssm_check_status.restype = i32
             L.ssm_check_status.argtypes = [vp]
             L.ssm_status_string.restype = ctypes.c_char_p
@@ -120,6 +133,13 @@ def call_bwd(addrs, dims: SsmDims, stream) -> int:
     declaration order (0 = NULL)."""
     assert len(addrs) == 20
     return lib().ssm_selective_scan_bwd(*[a or None for a in addrs], ctypes.byref(dims), stream or None)
+
+
+def call_ssd(x, dt, A, B, C, D, z, dt_bias, out, final_state, dims: SsdDims, stream) -> int:
+    """Raw call of ssm_ssd_fwd (integer addresses, 0 = NULL)."""
+    return lib().ssm_ssd_fwd(x or None, dt or None, A or None, B or None, C or None, D or None,
+                             z or None, dt_bias or None, out or None, final_state or None,
+                             ctypes.byref(dims), stream or None)
 
 
 def check_status(stream=0) -> int:

@@ -37,7 +37,7 @@ def sources():
 
 def headers():
     return (sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")))
-            + [os.path.join(ROOT, "include", "ssm_scan.h")])
+            + sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
 
 
 def _compile(src: str, verbose: bool) -> str:

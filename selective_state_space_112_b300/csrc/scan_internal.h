@@ -25,4 +25,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
                  float* final_state, const ssm_dims* dims, cudaStream_t stream, void* scratch,
                  size_t scratch_bytes, const ConvPrologue* conv);
 
+// Counts one kernel launch of the library (read by ssm_kernel_launches).
+void count_launch();
+
 }  // namespace ssm_internal

@@ -1,0 +1,545 @@
+// Mamba-2 SSD layer, forward: the scan with one scalar decay per head, evaluated
+// chunk by chunk in its dual (masked-attention) form on the tensor cores.
+//
+// Pages: "State-space models", section "The parallel scan" (A a scalar times the
+// identity per head turns the scan into blocks of matrix products); "Structured
+// State Space Models and Mamba", section "State Space Duality and Mamba-2"
+// (Y = (L o (Q K^T)) V with a 1-semiseparable decay mask L).
+//
+// One CTA owns one (batch row, head, block of PB channels) and walks its sequence in
+// chunks of Q = 64 steps, carrying that (N, PB) part of the state in fp32 registers.  With S_i the
+// running sum of step * A inside the chunk, for steps i, j of the chunk:
+//   M[i][j]   = (C_i . B_j) exp(S_i - S_j) step_j            j <= i, else 0
+//   y_i       = exp(S_i) C_i . h_prev  +  sum_j M[i][j] x_j  +  D x_i
+//   h_next    = exp(S_last) h_prev  +  sum_j B_j (exp(S_last - S_j) step_j x_j)^T
+// Four products per chunk on the tensor cores (bf16 operands, fp32 accumulation):
+// C B^T (Q x Q over N), C h_prev (Q x PB over N), M X (Q x PB over Q) and
+// B^T Xw (N x PB over Q).  The operands formed inside the kernel in fp32 (M, Xw and
+// the carried state) enter as a pair of bf16 values, hi = bf16(v) and
+// lo = bf16(v - hi), with one product each: about 16 significant bits, where one
+// bf16 rounding (8 bits) of the state would show in y at the 1e-2 level.  C, B and x
+// are bf16 inputs and exact.  Inputs stream through a two-stage cp.async ring.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "scan_internal.h"
+#include "ssm_ssd.h"
+
+namespace {
+
+constexpr int Q = 64;          // chunk length in steps
+constexpr int P = 64;          // channels per head
+constexpr int NWARP = 8;
+constexpr int NTHR = NWARP * 32;
+
+template <int N, int PB>
+struct SsdSmem {
+  static constexpr int XS = PB + 8;  // row stride (bf16 elements) of the x, Xw and state tiles
+  static constexpr int MS = Q + 8;   // row stride of the M tile
+  static constexpr int BS = N + 8;   // row stride of the B and C tiles
+  static constexpr int YS = PB + 4;  // row stride (fp32) of the y tile
+  static constexpr int X_BYTES = Q * XS * 2;
+  static constexpr int M_BYTES = Q * MS * 2;
+  static constexpr int S_BYTES = N * XS * 2;
+  static constexpr int BC_BYTES = Q * BS * 2;
+  static constexpr int STAGE = X_BYTES + 2 * BC_BYTES;  // x, B, C of one chunk
+  static constexpr int OFF_M = 2 * STAGE;                // M hi, M lo
+  static constexpr int OFF_XW = OFF_M + 2 * M_BYTES;     // Xw hi, Xw lo
+  static constexpr int OFF_Y = OFF_XW + 2 * X_BYTES;
+  static constexpr int OFF_S = OFF_Y + Q * YS * 4;       // state hi, state lo
+  static constexpr int OFF_V = OFF_S + 2 * S_BYTES;      // per-step vectors
+  static constexpr int BYTES = OFF_V + 4 * Q * 4;
+};
+
+struct SsdParams {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* dt;
+  const __nv_bfloat16* B;
+  const __nv_bfloat16* C;
+  const __nv_bfloat16* z;
+  const float* A;
+  const float* D;
+  const float* dt_bias;
+  __nv_bfloat16* out;
+  float* state;
+  int64_t L;
+  int H, G, hpg;  // heads, groups, heads per group
+  int softplus, state_in;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte global -> shared copy; ok == false fills the 16 bytes with zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += a (16 x 16, row) * b (16 x 8, col), bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Addresses of one lane for an ldmatrix.x4 (stride in bf16 elements).
+// A operand, 16 x 16 at (m0, k0) of a [m][k] tile.
+__device__ __forceinline__ uint32_t a_addr(uint32_t base, int stride, int m0, int k0, int lane) {
+  return base + 2u * ((m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * stride + k0 + (lane >> 4) * 8);
+}
+// A operand, 16 x 16 at (m0, k0), from a [k][m] tile (transposing load).
+__device__ __forceinline__ uint32_t a_addr_t(uint32_t base, int stride, int m0, int k0, int lane) {
+  return base + 2u * ((k0 + (lane & 7) + (lane >> 4) * 8) * stride + m0 + ((lane >> 3) & 1) * 8);
+}
+// B operands of the two 8-wide column tiles n0, n0 + 8 over k0..k0+15, from a [n][k] tile.
+__device__ __forceinline__ uint32_t b_addr(uint32_t base, int stride, int n0, int k0, int lane) {
+  return base + 2u * ((n0 + (lane & 7) + (lane >> 4) * 8) * stride + k0 + ((lane >> 3) & 1) * 8);
+}
+// The same from a [k][n] tile (transposing load).
+__device__ __forceinline__ uint32_t b_addr_t(uint32_t base, int stride, int n0, int k0, int lane) {
+  return base + 2u * ((k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * stride + n0 + (lane >> 4) * 8);
+}
+
+__device__ __forceinline__ float softplus_f(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+
+// v = hi + lo with both parts bf16 (lo holds what hi rounds away)
+__device__ __forceinline__ void split2(float a, float b, __nv_bfloat162& hi, __nv_bfloat162& lo) {
+  hi = __floats2bfloat162_rn(a, b);
+  const float2 h = __bfloat1622float2(hi);
+  lo = __floats2bfloat162_rn(a - h.x, b - h.y);
+}
+__device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+
+template <int N, int PB>
+__global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
+  using Sm = SsdSmem<N, PB>;
+  constexpr int XS = Sm::XS, MS = Sm::MS, BS = Sm::BS, YS = Sm::YS;
+  constexpr int YNT = PB / 16;  // 8-column tiles of y per warp (two warps across PB)
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, cq = lane & 3;
+  const int h = blockIdx.x / (P / PB), pc = (blockIdx.x % (P / PB)) * PB;  // head, first channel
+  const int b = blockIdx.y, g = h / p.hpg;
+  const int64_t L = p.L;
+  const int nch = (int)((L + Q - 1) / Q);
+  const float Ah = p.A[h];
+  const float Dh = p.D ? p.D[h] : 0.f;
+  const float biash = p.dt_bias ? p.dt_bias[h] : 0.f;
+
+  float* cumS = reinterpret_cast<float*>(smem + Sm::OFF_V);  // S_i
+  float* eS = cumS + Q;                                       // exp(S_i)
+  float* wS = eS + Q;                                         // exp(S_last - S_j) step_j
+  float* sS = wS + Q;                                         // step_j
+  __nv_bfloat16* Ms = reinterpret_cast<__nv_bfloat16*>(smem + Sm::OFF_M);    // hi; lo follows
+  __nv_bfloat16* Xws = reinterpret_cast<__nv_bfloat16*>(smem + Sm::OFF_XW);  // hi; lo follows
+  float* Ys = reinterpret_cast<float*>(smem + Sm::OFF_Y);
+  __nv_bfloat16* Ss = reinterpret_cast<__nv_bfloat16*>(smem + Sm::OFF_S);    // state [n][p], hi; lo follows
+  constexpr int M_LO = Sm::M_BYTES / 2, X_LO = Sm::X_BYTES / 2, S_LO = Sm::S_BYTES / 2;  // in elements
+
+  // chunk c's x, B and C rows into stage c % 2 (rows past the end are zeros)
+  auto issue = [&](int c) {
+    unsigned char* st = smem + (c & 1) * Sm::STAGE;
+    const int64_t t0 = (int64_t)c * Q;
+    for (int i = tid; i < Q * (PB / 8); i += NTHR) {
+      const int r = i / (PB / 8), k = i % (PB / 8);
+      const bool ok = t0 + r < L;
+      const int64_t t = ok ? t0 + r : t0;
+      cp_async16(smem_u32(st + (r * XS + k * 8) * 2),
+                 p.x + (((int64_t)b * L + t) * p.H + h) * P + pc + k * 8, ok);
+    }
+    for (int i = tid; i < Q * (N / 8); i += NTHR) {
+      const int r = i / (N / 8), k = i % (N / 8);
+      const bool ok = t0 + r < L;
+      const int64_t t = ok ? t0 + r : t0;
+      const int64_t off = (((int64_t)b * L + t) * p.G + g) * N + k * 8;
+      cp_async16(smem_u32(st + Sm::X_BYTES + (r * BS + k * 8) * 2), p.B + off, ok);
+      cp_async16(smem_u32(st + Sm::X_BYTES + Sm::BC_BYTES + (r * BS + k * 8) * 2), p.C + off, ok);
+    }
+  };
+
+  // the state tile of this warp: WM warps along N, WN along the CTA's PB channels
+  constexpr int WM = (N / 16 < NWARP) ? N / 16 : NWARP;
+  constexpr int WN = NWARP / WM;
+  constexpr int SMT = N / 16 / WM;  // 16-row tiles per warp
+  constexpr int SNT = PB / 8 / WN;  // 8-column tiles per warp
+  static_assert(SNT % 2 == 0, "column tiles are loaded in pairs");
+  const int sm0 = (warp % WM) * SMT * 16;
+  const int sn0 = (warp / WM) * SNT * 8;
+  float sacc[SMT][SNT][4];
+  const int64_t sbase = ((int64_t)b * p.H + h) * P * N;  // (b, h) block of the (b, H, P, N) state
+#pragma unroll
+  for (int mt = 0; mt < SMT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < SNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int n = sm0 + mt * 16 + gq + (e >> 1) * 8, pp = sn0 + nt * 8 + 2 * cq + (e & 1);
+        sacc[mt][nt][e] = p.state_in ? p.state[sbase + (int64_t)(pc + pp) * N + n] : 0.f;
+      }
+  // the state as the bf16 hi / lo operands of the next chunk's readout
+  auto store_state = [&]() {
+#pragma unroll
+    for (int mt = 0; mt < SMT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < SNT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int n = sm0 + mt * 16 + gq + hh * 8, pp = sn0 + nt * 8 + 2 * cq;
+          __nv_bfloat162 hi, lo;
+          split2(sacc[mt][nt][2 * hh], sacc[mt][nt][2 * hh + 1], hi, lo);
+          *reinterpret_cast<__nv_bfloat162*>(Ss + n * XS + pp) = hi;
+          *reinterpret_cast<__nv_bfloat162*>(Ss + S_LO + n * XS + pp) = lo;
+        }
+  };
+  bool have_state = p.state_in != 0;
+  if (have_state) store_state();
+
+  issue(0);
+  cp_async_commit();
+  if (nch > 1) issue(1);
+  cp_async_commit();
+
+  for (int c = 0; c < nch; ++c) {
+    cp_async_wait1();
+    __syncthreads();  // chunk c resident; the previous chunk's readers are done
+    const unsigned char* st = smem + (c & 1) * Sm::STAGE;
+    const uint32_t xs_u = smem_u32(st), bs_u = smem_u32(st + Sm::X_BYTES),
+                   cs_u = smem_u32(st + Sm::X_BYTES + Sm::BC_BYTES);
+    const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(st);
+    const int64_t t0 = (int64_t)c * Q;
+
+    if (warp == 0) {
+      // step sizes and running sums S_i of step * A over the chunk, two steps per lane
+      float stp[2], a2[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int64_t t = t0 + 2 * lane + k;
+        float s = 0.f;  // steps past the end: identity
+        if (t < L) {
+          const float v = __bfloat162float(p.dt[((int64_t)b * L + t) * p.H + h]) + biash;
+          s = p.softplus ? softplus_f(v) : v;
+        }
+        stp[k] = s;
+        a2[k] = s * Ah;
+      }
+      float incl = a2[0] + a2[1];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const float c1 = incl, c0 = incl - a2[1];
+      const float clast = __shfl_sync(0xffffffffu, incl, 31);
+      cumS[2 * lane] = c0;
+      cumS[2 * lane + 1] = c1;
+      eS[2 * lane] = expf(c0);
+      eS[2 * lane + 1] = expf(c1);
+      wS[2 * lane] = expf(clast - c0) * stp[0];
+      wS[2 * lane + 1] = expf(clast - c1) * stp[1];
+      sS[2 * lane] = stp[0];
+      sS[2 * lane + 1] = stp[1];
+    }
+    __syncthreads();
+
+    // Xw[j][p] = x[j][p] exp(S_last - S_j) step_j: the inputs weighted by their decay
+    // to the chunk end (hi / lo)
+    for (int i = tid; i < Q * (PB / 8); i += NTHR) {
+      const int r = i / (PB / 8), k = i % (PB / 8);
+      const uint4 v = *reinterpret_cast<const uint4*>(Xs + r * XS + k * 8);
+      const float wr = wS[r];
+      const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+      uint4 vh, vl;
+      __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&vh);
+      __nv_bfloat162* pl = reinterpret_cast<__nv_bfloat162*>(&vl);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(pv[e]);
+        split2(f.x * wr, f.y * wr, ph[e], pl[e]);
+      }
+      *reinterpret_cast<uint4*>(Xws + r * XS + k * 8) = vh;
+      *reinterpret_cast<uint4*>(Xws + X_LO + r * XS + k * 8) = vl;
+    }
+    // M = (C B^T) o decay mask o step: warp (mt, nh) takes rows 16 mt.., columns 32 nh..
+    {
+      const int i0 = (warp & 3) * 16, j0 = (warp >> 2) * 32;
+      if (j0 <= i0 + 15) {  // blocks wholly above the diagonal are never read
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll 4
+        for (int k0 = 0; k0 < N; k0 += 16) {
+          uint32_t a[4];
+          ldsm4(a_addr(cs_u, BS, i0, k0, lane), a);
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            uint32_t bb[4];
+            ldsm4(b_addr(bs_u, BS, j0 + np * 16, k0, lane), bb);
+            mma16816(acc[2 * np], a, bb[0], bb[1]);
+            mma16816(acc[2 * np + 1], a, bb[2], bb[3]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int i = i0 + gq + hh * 8, j = j0 + nt * 8 + 2 * cq;
+            const float ci = cumS[i];
+            const float v0 = (j <= i) ? acc[nt][2 * hh] * expf(ci - cumS[j]) * sS[j] : 0.f;
+            const float v1 = (j + 1 <= i) ? acc[nt][2 * hh + 1] * expf(ci - cumS[j + 1]) * sS[j + 1] : 0.f;
+            __nv_bfloat162 hi, lo;
+            split2(v0, v1, hi, lo);
+            *reinterpret_cast<__nv_bfloat162*>(Ms + i * MS + j) = hi;
+            *reinterpret_cast<__nv_bfloat162*>(Ms + M_LO + i * MS + j) = lo;
+          }
+      }
+    }
+    __syncthreads();
+
+    // y = exp(S_i) C_i . h_prev + M x + D x: warp (mt, nh) takes rows 16 mt.., channels
+    // PB / 2 nh..
+    {
+      const int i0 = (warp & 3) * 16, p0 = (warp >> 2) * (PB / 2);
+      float acc[YNT][4];
+#pragma unroll
+      for (int nt = 0; nt < YNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+      if (have_state) {
+        const uint32_t ss_u = smem_u32(Ss);
+#pragma unroll 4
+        for (int k0 = 0; k0 < N; k0 += 16) {
+          uint32_t a[4];
+          ldsm4(a_addr(cs_u, BS, i0, k0, lane), a);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)  // state hi, lo
+#pragma unroll
+            for (int np = 0; np < YNT / 2; ++np) {
+              uint32_t bb[4];
+              ldsm4_t(b_addr_t(ss_u + part * Sm::S_BYTES, XS, p0 + np * 16, k0, lane), bb);
+              mma16816(acc[2 * np], a, bb[0], bb[1]);
+              mma16816(acc[2 * np + 1], a, bb[2], bb[3]);
+            }
+        }
+        const float e0 = eS[i0 + gq], e1 = eS[i0 + gq + 8];
+#pragma unroll
+        for (int nt = 0; nt < YNT; ++nt) {
+          acc[nt][0] *= e0;
+          acc[nt][1] *= e0;
+          acc[nt][2] *= e1;
+          acc[nt][3] *= e1;
+        }
+      }
+      const uint32_t ms_u = smem_u32(Ms);
+      for (int k0 = 0; k0 <= i0; k0 += 16) {  // causal: columns past the row block are zero
+        uint32_t bx[YNT / 2][4];
+#pragma unroll
+        for (int np = 0; np < YNT / 2; ++np) ldsm4_t(b_addr_t(xs_u, XS, p0 + np * 16, k0, lane), bx[np]);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // M hi, lo
+          uint32_t a[4];
+          ldsm4(a_addr(ms_u + part * Sm::M_BYTES, MS, i0, k0, lane), a);
+#pragma unroll
+          for (int np = 0; np < YNT / 2; ++np) {
+            mma16816(acc[2 * np], a, bx[np][0], bx[np][1]);
+            mma16816(acc[2 * np + 1], a, bx[np][2], bx[np][3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < YNT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = i0 + gq + hh * 8, pp = p0 + nt * 8 + 2 * cq;
+          const float2 xv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Xs + i * XS + pp));
+          *reinterpret_cast<float2*>(Ys + i * YS + pp) =
+              make_float2(fmaf(Dh, xv.x, acc[nt][2 * hh]), fmaf(Dh, xv.y, acc[nt][2 * hh + 1]));
+        }
+    }
+    // h_next = exp(S_last) h_prev + B^T Xw
+    {
+      const float dl = eS[Q - 1];
+      const uint32_t xw_u = smem_u32(Xws);
+#pragma unroll
+      for (int mt = 0; mt < SMT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < SNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] *= dl;
+#pragma unroll
+      for (int k0 = 0; k0 < Q; k0 += 16) {
+        uint32_t a[SMT][4];
+#pragma unroll
+        for (int mt = 0; mt < SMT; ++mt) ldsm4_t(a_addr_t(bs_u, BS, sm0 + mt * 16, k0, lane), a[mt]);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)  // Xw hi, lo
+#pragma unroll
+          for (int np = 0; np < SNT / 2; ++np) {
+            uint32_t bb[4];
+            ldsm4_t(b_addr_t(xw_u + part * Sm::X_BYTES, XS, sn0 + np * 16, k0, lane), bb);
+#pragma unroll
+            for (int mt = 0; mt < SMT; ++mt) {
+              mma16816(sacc[mt][2 * np], a[mt], bb[0], bb[1]);
+              mma16816(sacc[mt][2 * np + 1], a[mt], bb[2], bb[3]);
+            }
+          }
+      }
+    }
+    __syncthreads();  // every read of this stage, of M, Xw and of the state tile is done
+
+    if (c + 2 < nch) issue(c + 2);
+    cp_async_commit();
+
+    // out = y silu(z), 8 channels per thread and piece
+    for (int i = tid; i < Q * (PB / 8); i += NTHR) {
+      const int r = i / (PB / 8), k = i % (PB / 8);
+      const int64_t t = t0 + r;
+      if (t >= L) continue;
+      const int64_t off = (((int64_t)b * L + t) * p.H + h) * P + pc + k * 8;
+      const float4 y0 = *reinterpret_cast<const float4*>(Ys + r * YS + k * 8);
+      const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * YS + k * 8 + 4);
+      float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      if (p.z) {
+        const uint4 zv = __ldg(reinterpret_cast<const uint4*>(p.z + off));
+        const __nv_bfloat162* zp = reinterpret_cast<const __nv_bfloat162*>(&zv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(zp[e]);
+          y[2 * e] *= silu_f(f.x);
+          y[2 * e + 1] *= silu_f(f.y);
+        }
+      }
+      uint4 o;
+      __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) op[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+      *reinterpret_cast<uint4*>(p.out + off) = o;
+    }
+    store_state();
+    have_state = true;
+  }
+
+  if (p.state) {
+#pragma unroll
+    for (int mt = 0; mt < SMT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < SNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = sm0 + mt * 16 + gq + (e >> 1) * 8, pp = sn0 + nt * 8 + 2 * cq + (e & 1);
+          p.state[sbase + (int64_t)(pc + pp) * N + n] = sacc[mt][nt][e];
+        }
+  }
+}
+
+template <int N, int PB>
+int launch_ssd(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
+  // the dynamic shared-memory limit is raised once per device
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(ready.load() & bit)) {
+    if (cudaFuncSetAttribute(ssd_fwd_kernel<N, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SsdSmem<N, PB>::BYTES) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    ready.fetch_or(bit);
+  }
+  ssd_fwd_kernel<N, PB><<<dim3((unsigned)prm.H * (P / PB), (unsigned)batch), NTHR, SsdSmem<N, PB>::BYTES,
+                          stream>>>(prm);
+  ssm_internal::count_launch();
+  return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* dt_bias, void* out,
+                           float* final_state, const ssm_ssd_dims* dims, cudaStream_t stream) {
+  if (!dims) return SSM_ERR_NULL;
+  const ssm_ssd_dims d = *dims;
+  if (d.batch <= 0 || d.batch > 65535 || d.seqlen < 0 || d.nheads <= 0 || d.nheads > (1 << 29) ||
+      d.headdim <= 0 || d.ngroups <= 0 || d.dstate <= 0 || d.nheads % d.ngroups != 0 ||
+      (d.io_dtype != SSM_F32 && d.io_dtype != SSM_BF16) || (d.dt_softplus != 0 && d.dt_softplus != 1) ||
+      (d.state_in != 0 && d.state_in != 1) || d.reserved != 0)
+    return SSM_ERR_DIMS;
+  if (d.state_in && !final_state) return SSM_ERR_DIMS;
+  if (d.seqlen > 0 && (!x || !dt || !A || !B || !C || !out)) return SSM_ERR_NULL;
+  const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, final_state};
+  for (const void* q : ptrs)
+    if ((uintptr_t)q % 16) return SSM_ERR_ALIGN;
+  if (d.io_dtype != SSM_BF16 || d.headdim != P ||
+      (d.dstate != 64 && d.dstate != 128 && d.dstate != 256))
+    return SSM_ERR_UNSUPPORTED;
+
+  const size_t act = (size_t)d.batch * d.seqlen * d.nheads * d.headdim * 2;
+  const size_t bc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate * 2;
+  const size_t st = (size_t)d.batch * d.nheads * d.headdim * d.dstate * 4;
+  const size_t hv = (size_t)d.nheads * 4;
+  const struct { const void* p; size_t n; } ins[] = {
+      {x, act}, {dt, (size_t)d.batch * d.seqlen * d.nheads * 2}, {A, hv}, {B, bc}, {C, bc},
+      {D, hv}, {z, act}, {dt_bias, hv}};
+  for (const auto& in : ins) {
+    if (overlap(out, act, in.p, in.n)) return SSM_ERR_OVERLAP;
+    if (overlap(final_state, st, in.p, in.n)) return SSM_ERR_OVERLAP;
+  }
+  if (overlap(final_state, st, out, act)) return SSM_ERR_OVERLAP;
+
+  if (d.seqlen == 0) {
+    if (final_state && !d.state_in && cudaMemsetAsync(final_state, 0, st, stream) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+
+  SsdParams prm;
+  memset(&prm, 0, sizeof prm);
+  prm.x = static_cast<const __nv_bfloat16*>(x);
+  prm.dt = static_cast<const __nv_bfloat16*>(dt);
+  prm.B = static_cast<const __nv_bfloat16*>(B);
+  prm.C = static_cast<const __nv_bfloat16*>(C);
+  prm.z = static_cast<const __nv_bfloat16*>(z);
+  prm.A = A;
+  prm.D = D;
+  prm.dt_bias = dt_bias;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.state = final_state;
+  prm.L = d.seqlen;
+  prm.H = (int)d.nheads;
+  prm.G = (int)d.ngroups;
+  prm.hpg = (int)(d.nheads / d.ngroups);
+  prm.softplus = d.dt_softplus;
+  prm.state_in = d.state_in;
+  switch (d.dstate) {
+    case 64: return launch_ssd<64, 64>(prm, d.batch, stream);
+    case 128: return launch_ssd<128, 64>(prm, d.batch, stream);
+    default: return launch_ssd<256, 32>(prm, d.batch, stream);  // half a head per CTA
+  }
+}

@@ -327,6 +327,8 @@ const char* ssm_status_string(int code) {
 
 namespace ssm_internal {
 
+void count_launch() { g_launches.fetch_add(1); }
+
 // The whole call.  scratch == nullptr: the chunk-carry workspace comes from the
 // library's stream-ordered pool.  Otherwise it is carved from `scratch`
 // (scratch_bytes long, device memory the caller keeps), nothing is allocated, and a

@@ -1,6 +1,6 @@
 """C-ABI checks that need no GPU: the library builds and loads, exports every
-function include/ssm_scan.h declares, and rejects bad arguments on the host
-before touching the device."""
+function include/*.h declares, and rejects bad arguments on the host before
+touching the device."""
 import os
 import re
 
@@ -9,13 +9,20 @@ import pytest
 from selective_state_space_112_b300 import _abi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("ssm_scan.h", "ssm_ssd.h")]
 
 
 def header_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", src)))
+    names = set()
+    for hdr in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
+        names.update(re.findall(r"\b(ssm_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_header_is_checked():
+    assert sorted(HEADERS) == sorted(
+        os.path.join(ROOT, "include", h) for h in os.listdir(os.path.join(ROOT, "include")) if h.endswith(".h"))
 
 
 def test_library_exports_every_declared_function():
@@ -153,3 +160,57 @@ def test_options():
     _abi.set_option("pow_path", 1)
     _abi.set_option("tma", 1)
     assert _abi.profile_read() == {}
+
+
+# ---------------------------------------------------------------- Mamba-2 SSD entry
+
+SP = {k: BASE + (20 + i) * (1 << 30) for i, k in enumerate(
+    ["x", "dt", "A", "B", "C", "D", "z", "bias", "out", "fs"])}
+
+
+def sdims(**kw):
+    base = dict(batch=2, seqlen=100, nheads=4, headdim=64, ngroups=2, dstate=128, io_dtype=1,
+                dt_softplus=1, state_in=0, reserved=0)
+    base.update(kw)
+    return _abi.SsdDims(**base)
+
+
+def call_ssd(d, **over):
+    q = dict(SP)
+    q.update(over)
+    return _abi.call_ssd(q["x"], q["dt"], q["A"], q["B"], q["C"], q["D"], q["z"], q["bias"],
+                         q["out"], q["fs"], d, 0)
+
+
+def test_ssd_entry_host_checks():
+    """ssm_ssd_fwd rejects bad arguments on the host: NULL dims and required
+    pointers, bad sizes and flags, misaligned pointers, overlapping outputs, and the
+    forms this build does not cover (fp32 io, head dimension other than 64, N other
+    than 64, 128 or 256)."""
+    L = _abi.lib()
+    assert L.ssm_ssd_fwd(*([None] * 10), None, None) == -1
+    for k in ("x", "dt", "A", "B", "C", "out"):
+        assert call_ssd(sdims(), **{k: 0}) == -1, k
+    for bad in (dict(batch=0), dict(batch=65536), dict(seqlen=-1), dict(nheads=0), dict(headdim=0),
+                dict(ngroups=0), dict(ngroups=3), dict(dstate=0), dict(io_dtype=2),
+                dict(dt_softplus=2), dict(state_in=2), dict(reserved=1)):
+        assert call_ssd(sdims(**bad)) == -2, bad
+    assert call_ssd(sdims(state_in=1), fs=0) == -2
+    for k in SP:
+        assert call_ssd(sdims(), **{k: SP[k] + 4}) == -3, k
+    assert call_ssd(sdims(), out=SP["x"] + 16) == -6
+    assert call_ssd(sdims(), fs=SP["out"]) == -6
+    assert call_ssd(sdims(), fs=SP["B"]) == -6
+    for bad in (dict(io_dtype=0), dict(headdim=32), dict(dstate=16), dict(dstate=96)):
+        assert call_ssd(sdims(**bad)) == -4, bad
+
+
+def test_ssd_entry_reaches_the_device():
+    """A valid SSD call passes host validation (N 64, 128, 256, with and without
+    groups): without a GPU it fails only at the device (SSM_ERR_CUDA)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for n in (64, 128, 256):
+        assert call_ssd(sdims(dstate=n)) == -5, n
+    assert call_ssd(sdims(ngroups=1, D=0, z=0, bias=0, fs=0)) == -5
