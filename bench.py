@@ -250,6 +250,8 @@ def main():
                     help="the Mamba-block prologue (causal conv of width 4 + silu) fused in")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (gradients of every input) instead")
+    ap.add_argument("--ssd", action="store_true",
+                    help="time the Mamba-2 SSD layer (default workload mamba2_2p7b_bf16) instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -257,7 +259,13 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from selective_state_space_112_b300.workloads import CONFIGS, make_workload
+    from selective_state_space_112_b300.workloads import CONFIGS, SSD_CONFIGS, make_workload
+    if args.ssd:
+        if args.workload not in SSD_CONFIGS:
+            args.workload = "mamba2_2p7b_bf16"
+        if args.impl == "reference":
+            return reference_arm(args, world, rank)
+        return ssd_bench(args, world, rank, local)
     if args.workload not in CONFIGS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(CONFIGS)}")
 
@@ -593,11 +601,184 @@ def cpu_baseline_bwd(w, dout, budget_s: float = 15.0):
                       f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
 
 
+SSD_Q = 64  # chunk length of the SSD kernel's dual form
+
+
+def ssd_algorithmic(w):
+    """Bytes and multiply-add flops one SSD call must move / do at least.
+    Bytes: x, z in and out once (b L H P, bf16), dt (b L H), B and C (b L G N), the
+    per-head parameters and the final state (b H P N fp32).  Flops: the dual form per
+    64-step chunk and head: the causal half of C B^T (Q(Q+1)/2 N) and of M x
+    (Q(Q+1)/2 P), the readout of the carried state C h (Q P N) and its update B^T x
+    (N P Q), two flops per multiply-add."""
+    tc = w.batch * w.seqlen * w.nheads * w.headdim
+    byt = (tc * 2 * (3 if w.z is not None else 2) + w.batch * w.seqlen * w.nheads * 2
+           + 2 * w.batch * w.seqlen * w.ngroups * w.dstate * 2 + 3 * w.nheads * 4
+           + w.batch * w.nheads * w.headdim * w.dstate * 4)
+    Q, P, N = SSD_Q, w.headdim, w.dstate
+    nch = (w.seqlen + Q - 1) // Q
+    flops = w.batch * w.nheads * nch * 2 * (Q * (Q + 1) // 2 * (N + P) + 2 * Q * P * N)
+    return byt, flops
+
+
+def ssd_bench(args, world, rank, local):
+    """One step = one ssm_ssd_fwd call over a Mamba-2-shaped layer (bf16 in and out,
+    fp32 state), inputs resident in HBM; e2e adds the host copies."""
+    import torch
+    import torch.distributed as dist
+    import selective_state_space_112_b300 as ssm
+    from selective_state_space_112_b300.workloads import SSD_CONFIGS, make_ssd
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    spec = dict(SSD_CONFIGS[args.workload])
+    spec["seed"] = spec["seed"] + 1000 * rank
+    w = make_ssd(args.workload, **spec)
+    names = ("x", "dt", "A", "B", "C", "D", "z", "dt_bias")
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    host = {k: (None if getattr(w, k) is None else
+                (bf(getattr(w, k)) if getattr(w, k).dtype == np.uint16 else torch.from_numpy(getattr(w, k))))
+            for k in names}
+    t = {k: (v.to(device) if v is not None else None) for k, v in host.items()}
+    out = torch.empty_like(t["x"])
+    fs = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call(d, o, f):
+        ssm.ssm_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                        out=o, final_state=f)
+
+    for _ in range(args.warmup):
+        call(t, out, fs)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ssm.ssm_kernel_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            call(t, out, fs)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    launches = ssm.ssm_kernel_launches() - launches0
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        ms = max_over_ranks(ms, dist, device)
+        dist.barrier()
+    ms_step = ms / args.steps
+    units = w.tokens_channels
+    value = job_throughput(units, args.steps, ms, world)
+    byt, flops = ssd_algorithmic(w)
+    hbm_peak, _, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc_peak, tc_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tc_peak, tc_kind = 1800.0, "fallback"
+    # one kernel launch per step: the step's event time is the kernel's duration
+    hbm_ach = byt / (ms_step * 1e-3) / 1e9
+    tc_ach = flops / (ms_step * 1e-3) / 1e12
+    t_hbm, t_tc = byt / (hbm_peak * 1e9), flops / (tc_peak * 1e12)
+    hbm_obj = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": hbm_peak, "unit": "GB/s",
+               "frac": round(hbm_ach / hbm_peak, 4), "peak_source": peak_kind}
+    tc_obj = {"bound": "tensor", "achieved": round(tc_ach, 2), "peak": tc_peak, "unit": "TFLOP/s",
+              "frac": round(tc_ach / tc_peak, 4), "peak_source": f"{tc_kind} bf16 burst"}
+    main_obj, other = (hbm_obj, tc_obj) if t_hbm >= t_tc else (tc_obj, hbm_obj)
+    roof = dict(main_obj, kernel="ssd_fwd_kernel", traffic=None, algorithmic_bytes_per_launch=byt,
+                algorithmic_flops_per_launch=flops, kernel_ms_avg=round(ms_step, 4),
+                roofline_ms={"hbm": round(t_hbm * 1e3, 4), "tensor": round(t_tc * 1e3, 4)},
+                other=other)
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": args.workload, "layer": "Mamba-2 SSD", "batch": w.batch,
+                      "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+                      "ngroups": w.ngroups, "dstate": w.dstate, "gate": w.z is not None,
+                      "parallelism": f"replica x{world}" if world > 1 else "single",
+                      "l2": f"inputs {byt / 1e9:.2f} GB > 126 MB L2; no flush needed"},
+           "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary()}
+    if not args.no_e2e:
+        hp = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+        dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in hp.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
+
+        def e2e_step():
+            for k, v in hp.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            call(dev_in, out, fs)
+            out_h.copy_(out, non_blocking=True)
+            fs_h.copy_(fs, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            ems = max_over_ranks(ems, dist, device)
+        res["e2e"] = {"value": job_throughput(units, args.e2e_steps, ems, world), "unit": UNIT,
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": ems / args.e2e_steps}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_ssd(w)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def cpu_baseline_ssd(w, budget_s: float = 15.0):
+    """The float64 oracle's SSD recurrence on the first k heads of the first r batch
+    rows, whole sequence (k grows first, then r, to about budget_s of host time)."""
+    import oracle
+    cores = oracle.max_threads()
+    hpg = w.nheads // w.ngroups
+
+    def run(r, k):
+        g1 = (k - 1) // hpg + 1  # groups the first k heads read
+        sl = lambda a: None if a is None else np.ascontiguousarray(a[:r, :, :k])
+        t0 = time.perf_counter()
+        oracle.ssd(sl(w.x), sl(w.dt), w.A[:k], np.ascontiguousarray(w.B[:r, :, :g1]),
+                   np.ascontiguousarray(w.C[:r, :, :g1]), D=None if w.D is None else w.D[:k],
+                   z=sl(w.z), dt_bias=None if w.dt_bias is None else w.dt_bias[:k])
+        return time.perf_counter() - t0
+
+    r, k = 1, min(w.nheads, max(1, min(cores, 4)))
+    t = run(r, k)
+    k2 = int(min(w.nheads, max(k, k * budget_s / max(t, 1e-3))))
+    if k2 > k:
+        t, k = run(r, k2), k2
+    if k == w.nheads and t < budget_s / 2 and w.batch > 1:
+        r2 = int(min(w.batch, max(1, budget_s / max(t, 1e-3))))
+        if r2 > r:
+            t, r = run(r2, k), r2
+    units = r * k * w.headdim * w.seqlen
+    return {"value": units / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"SSD, heads 0..{k - 1} of batch rows 0..{r - 1}, all {w.seqlen} steps, "
+                      f"P={w.headdim}, N={w.dstate} ({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
+
+
 def reference_arm(args, world, rank):
     """The oracle as the reference arm: timed on the host cores, each step a
     bounded sample of the same workload.  Under torchrun only rank 0 runs."""
     if rank != 0:
         return
+    if getattr(args, "ssd", False):
+        return reference_arm_ssd(args, world)
     from selective_state_space_112_b300.workloads import config
     import oracle
     w = config(args.workload)
@@ -618,6 +799,33 @@ def reference_arm(args, world, rank):
                       "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                             "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps per step"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+
+def reference_arm_ssd(args, world):
+    """The SSD oracle as the reference arm: each step its bounded head sample."""
+    from selective_state_space_112_b300.workloads import SSD_CONFIGS, make_ssd
+    w = make_ssd(args.workload, **SSD_CONFIGS[args.workload])
+    el = units = 0.0
+    sample = None
+    for i in range(args.steps):
+        cb = cpu_baseline_ssd(w, budget_s=5.0)
+        units_i = float(cb["sample"].split("(")[1].split(" ")[0])
+        el += units_i / cb["value"]
+        units += units_i
+        sample, cores = cb["sample"], cb["cores"]
+    value = units / el
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "layer": "Mamba-2 SSD", "batch": w.batch,
+                      "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+                      "ngroups": w.ngroups, "dstate": w.dstate},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"{sample}, per step"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 

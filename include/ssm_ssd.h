@@ -74,9 +74,11 @@ typedef struct {
  * value, state_in without final_state), SSM_ERR_ALIGN, SSM_ERR_OVERLAP,
  * SSM_ERR_UNSUPPORTED (io dtype, headdim or dstate this build does not cover),
  * SSM_ERR_CUDA (launch failure or no usable device).
- * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation (the
- * masked decay matrix, the decay-weighted inputs and the carried state are
- * rounded to bf16 as operands); step sizes, decays and the state in fp32.
+ * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation.  The
+ * operands formed inside the kernel (the masked decay matrix, the decay-weighted
+ * inputs and the carried state, all fp32) enter as a pair of bf16 values (value
+ * and remainder), about 16 significant bits; step sizes, decays and the state
+ * are kept in fp32.
  */
 int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                 const float* D, const void* z, const float* dt_bias, void* out,

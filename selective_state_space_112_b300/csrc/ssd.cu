@@ -46,13 +46,17 @@ struct SsdSmem {
   static constexpr int M_BYTES = Q * MS * 2;
   static constexpr int S_BYTES = N * XS * 2;
   static constexpr int BC_BYTES = Q * BS * 2;
-  static constexpr int STAGE = X_BYTES + 2 * BC_BYTES;  // x, B, C of one chunk
+  // the gate z rides in the stage (x, B, C, z of one chunk) unless it would not fit
+  static constexpr bool Z_SMEM = 2 * (2 * X_BYTES + 2 * BC_BYTES) + 2 * Q * MS * 2 + 2 * X_BYTES +
+                                     Q * YS * 4 + 2 * N * XS * 2 + 8 * Q * 4 <= 232448;
+  static constexpr int OFF_Z = X_BYTES + 2 * BC_BYTES;
+  static constexpr int STAGE = (Z_SMEM ? 2 : 1) * X_BYTES + 2 * BC_BYTES;
   static constexpr int OFF_M = 2 * STAGE;                // M hi, M lo
   static constexpr int OFF_XW = OFF_M + 2 * M_BYTES;     // Xw hi, Xw lo
   static constexpr int OFF_Y = OFF_XW + 2 * X_BYTES;
   static constexpr int OFF_S = OFF_Y + Q * YS * 4;       // state hi, state lo
-  static constexpr int OFF_V = OFF_S + 2 * S_BYTES;      // per-step vectors
-  static constexpr int BYTES = OFF_V + 4 * Q * 4;
+  static constexpr int OFF_V = OFF_S + 2 * S_BYTES;      // per-step vectors, two chunks
+  static constexpr int BYTES = OFF_V + 8 * Q * 4;
 };
 
 struct SsdParams {
@@ -147,10 +151,9 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
   const float Dh = p.D ? p.D[h] : 0.f;
   const float biash = p.dt_bias ? p.dt_bias[h] : 0.f;
 
-  float* cumS = reinterpret_cast<float*>(smem + Sm::OFF_V);  // S_i
-  float* eS = cumS + Q;                                       // exp(S_i)
-  float* wS = eS + Q;                                         // exp(S_last - S_j) step_j
-  float* sS = wS + Q;                                         // step_j
+  // per-step vectors of a chunk (chunk c in buffer c % 2): S_i, exp(S_i),
+  // exp(S_last - S_j) step_j, step_j
+  float* const vbuf = reinterpret_cast<float*>(smem + Sm::OFF_V);
   __nv_bfloat16* Ms = reinterpret_cast<__nv_bfloat16*>(smem + Sm::OFF_M);    // hi; lo follows
   __nv_bfloat16* Xws = reinterpret_cast<__nv_bfloat16*>(smem + Sm::OFF_XW);  // hi; lo follows
   float* Ys = reinterpret_cast<float*>(smem + Sm::OFF_Y);
@@ -165,8 +168,9 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
       const int r = i / (PB / 8), k = i % (PB / 8);
       const bool ok = t0 + r < L;
       const int64_t t = ok ? t0 + r : t0;
-      cp_async16(smem_u32(st + (r * XS + k * 8) * 2),
-                 p.x + (((int64_t)b * L + t) * p.H + h) * P + pc + k * 8, ok);
+      const int64_t off = (((int64_t)b * L + t) * p.H + h) * P + pc + k * 8;
+      cp_async16(smem_u32(st + (r * XS + k * 8) * 2), p.x + off, ok);
+      if (Sm::Z_SMEM && p.z) cp_async16(smem_u32(st + Sm::OFF_Z + (r * XS + k * 8) * 2), p.z + off, ok);
     }
     for (int i = tid; i < Q * (N / 8); i += NTHR) {
       const int r = i / (N / 8), k = i % (N / 8);
@@ -215,6 +219,54 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
   bool have_state = p.state_in != 0;
   if (have_state) store_state();
 
+  // warp 0: the raw steps of chunk c, two per lane (read one chunk ahead of use)
+  auto load_dt = [&](int c, float (&r)[2]) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t t = (int64_t)c * Q + 2 * lane + k;
+      r[k] = (c < nch && t < L) ? __bfloat162float(p.dt[((int64_t)b * L + t) * p.H + h]) : 0.f;
+    }
+  };
+  // warp 0: step sizes and running sums S_i of step * A over chunk c
+  auto make_v = [&](int c, const float (&r)[2]) {
+    float* V = vbuf + (c & 1) * 4 * Q;
+    float stp[2], a2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t t = (int64_t)c * Q + 2 * lane + k;
+      float s = 0.f;  // steps past the end: identity
+      if (t < L) {
+        const float v = r[k] + biash;
+        s = p.softplus ? softplus_f(v) : v;
+      }
+      stp[k] = s;
+      a2[k] = s * Ah;
+    }
+    float incl = a2[0] + a2[1];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const float c1 = incl, c0 = incl - a2[1];
+    const float clast = __shfl_sync(0xffffffffu, incl, 31);
+    V[2 * lane] = c0;
+    V[2 * lane + 1] = c1;
+    V[Q + 2 * lane] = expf(c0);
+    V[Q + 2 * lane + 1] = expf(c1);
+    V[2 * Q + 2 * lane] = expf(clast - c0) * stp[0];
+    V[2 * Q + 2 * lane + 1] = expf(clast - c1) * stp[1];
+    V[3 * Q + 2 * lane] = stp[0];
+    V[3 * Q + 2 * lane + 1] = stp[1];
+  };
+  float dtn[2] = {0.f, 0.f};  // warp 0: raw steps of the next chunk
+  if (warp == 0) {
+    float r0[2];
+    load_dt(0, r0);
+    make_v(0, r0);
+    load_dt(1, dtn);
+  }
+
   issue(0);
   cp_async_commit();
   if (nch > 1) issue(1);
@@ -229,38 +281,10 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
     const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(st);
     const int64_t t0 = (int64_t)c * Q;
 
-    if (warp == 0) {
-      // step sizes and running sums S_i of step * A over the chunk, two steps per lane
-      float stp[2], a2[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int64_t t = t0 + 2 * lane + k;
-        float s = 0.f;  // steps past the end: identity
-        if (t < L) {
-          const float v = __bfloat162float(p.dt[((int64_t)b * L + t) * p.H + h]) + biash;
-          s = p.softplus ? softplus_f(v) : v;
-        }
-        stp[k] = s;
-        a2[k] = s * Ah;
-      }
-      float incl = a2[0] + a2[1];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      const float c1 = incl, c0 = incl - a2[1];
-      const float clast = __shfl_sync(0xffffffffu, incl, 31);
-      cumS[2 * lane] = c0;
-      cumS[2 * lane + 1] = c1;
-      eS[2 * lane] = expf(c0);
-      eS[2 * lane + 1] = expf(c1);
-      wS[2 * lane] = expf(clast - c0) * stp[0];
-      wS[2 * lane + 1] = expf(clast - c1) * stp[1];
-      sS[2 * lane] = stp[0];
-      sS[2 * lane + 1] = stp[1];
-    }
-    __syncthreads();
+    const float* cumS = vbuf + (c & 1) * 4 * Q;
+    const float* eS = cumS + Q;
+    const float* wS = eS + Q;
+    const float* sS = wS + Q;
 
     // Xw[j][p] = x[j][p] exp(S_last - S_j) step_j: the inputs weighted by their decay
     // to the chunk end (hi / lo)
@@ -409,10 +433,8 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
     }
     __syncthreads();  // every read of this stage, of M, Xw and of the state tile is done
 
-    if (c + 2 < nch) issue(c + 2);
-    cp_async_commit();
-
-    // out = y silu(z), 8 channels per thread and piece
+    // out = y silu(z), 8 channels per thread and piece (the same pieces this thread
+    // copies in, so the stage is read here before this thread refills it)
     for (int i = tid; i < Q * (PB / 8); i += NTHR) {
       const int r = i / (PB / 8), k = i % (PB / 8);
       const int64_t t = t0 + r;
@@ -422,7 +444,8 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
       const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * YS + k * 8 + 4);
       float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
       if (p.z) {
-        const uint4 zv = __ldg(reinterpret_cast<const uint4*>(p.z + off));
+        const uint4 zv = Sm::Z_SMEM ? *reinterpret_cast<const uint4*>(st + Sm::OFF_Z + (r * XS + k * 8) * 2)
+                                    : __ldg(reinterpret_cast<const uint4*>(p.z + off));
         const __nv_bfloat162* zp = reinterpret_cast<const __nv_bfloat162*>(&zv);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -437,8 +460,14 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
       for (int e = 0; e < 4; ++e) op[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
       *reinterpret_cast<uint4*>(p.out + off) = o;
     }
+    if (c + 2 < nch) issue(c + 2);
+    cp_async_commit();
     store_state();
     have_state = true;
+    if (warp == 0 && c + 1 < nch) {
+      make_v(c + 1, dtn);
+      load_dt(c + 2, dtn);
+    }
   }
 
   if (p.state) {
