@@ -133,7 +133,9 @@ __device__ __forceinline__ void split2(float a, float b, __nv_bfloat162& hi, __n
   const float2 h = __bfloat1622float2(hi);
   lo = __floats2bfloat162_rn(a - h.x, b - h.y);
 }
-__device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+// the gate and the decay mask take the hardware exponential (relative error near
+// 2^-21, far inside the 16-bit operands and the bf16 output)
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
 
 template <int N, int PB>
 __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
@@ -288,6 +290,8 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
 
     // Xw[j][p] = x[j][p] exp(S_last - S_j) step_j: the inputs weighted by their decay
     // to the chunk end (hi / lo)
+    static_assert(Q * (PB / 8) % NTHR == 0, "whole pieces per thread");
+#pragma unroll
     for (int i = tid; i < Q * (PB / 8); i += NTHR) {
       const int r = i / (PB / 8), k = i % (PB / 8);
       const uint4 v = *reinterpret_cast<const uint4*>(Xs + r * XS + k * 8);
@@ -331,8 +335,8 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
           for (int hh = 0; hh < 2; ++hh) {
             const int i = i0 + gq + hh * 8, j = j0 + nt * 8 + 2 * cq;
             const float ci = cumS[i];
-            const float v0 = (j <= i) ? acc[nt][2 * hh] * expf(ci - cumS[j]) * sS[j] : 0.f;
-            const float v1 = (j + 1 <= i) ? acc[nt][2 * hh + 1] * expf(ci - cumS[j + 1]) * sS[j + 1] : 0.f;
+            const float v0 = (j <= i) ? acc[nt][2 * hh] * __expf(ci - cumS[j]) * sS[j] : 0.f;
+            const float v1 = (j + 1 <= i) ? acc[nt][2 * hh + 1] * __expf(ci - cumS[j + 1]) * sS[j + 1] : 0.f;
             __nv_bfloat162 hi, lo;
             split2(v0, v1, hi, lo);
             *reinterpret_cast<__nv_bfloat162*>(Ms + i * MS + j) = hi;
@@ -342,19 +346,30 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
     }
     __syncthreads();
 
-    // y = exp(S_i) C_i . h_prev + M x + D x: warp (mt, nh) takes rows 16 mt.., channels
-    // PB / 2 nh..
+    // y = exp(S_i) C_i . h_prev + M x + D x (warp (mt, nh): rows 16 mt.., channels
+    // PB / 2 nh..) and h_next = exp(S_last) h_prev + B^T Xw, their k-steps interleaved
+    // so that three independent accumulator chains are in flight per warp
     {
       const int i0 = (warp & 3) * 16, p0 = (warp >> 2) * (PB / 2);
-      float acc[YNT][4];
+      const int mtw = warp & 3;  // the causal product takes k-steps 0..mtw
+      float acc[YNT][4], accd[YNT][4];  // C h_prev; M x
 #pragma unroll
       for (int nt = 0; nt < YNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-      if (have_state) {
-        const uint32_t ss_u = smem_u32(Ss);
-#pragma unroll 4
-        for (int k0 = 0; k0 < N; k0 += 16) {
+        for (int e = 0; e < 4; ++e) acc[nt][e] = accd[nt][e] = 0.f;
+      const float dl = eS[Q - 1];
+#pragma unroll
+      for (int mt = 0; mt < SMT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < SNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] *= dl;
+      const uint32_t ss_u = smem_u32(Ss), ms_u = smem_u32(Ms), xw_u = smem_u32(Xws);
+      constexpr int KN = N / 16, KQ = Q / 16, KMAX = KN > KQ ? KN : KQ;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int k0 = k * 16;
+        if (k < KN && have_state) {  // C h_prev over states k0..k0+15
           uint32_t a[4];
           ldsm4(a_addr(cs_u, BS, i0, k0, lane), a);
 #pragma unroll
@@ -367,69 +382,51 @@ __global__ void __launch_bounds__(NTHR, 1) ssd_fwd_kernel(const SsdParams p) {
               mma16816(acc[2 * np + 1], a, bb[2], bb[3]);
             }
         }
-        const float e0 = eS[i0 + gq], e1 = eS[i0 + gq + 8];
+        if (k < KQ && k <= mtw) {  // M x over steps k0..k0+15 (causal)
+          uint32_t bx[YNT / 2][4];
 #pragma unroll
-        for (int nt = 0; nt < YNT; ++nt) {
-          acc[nt][0] *= e0;
-          acc[nt][1] *= e0;
-          acc[nt][2] *= e1;
-          acc[nt][3] *= e1;
-        }
-      }
-      const uint32_t ms_u = smem_u32(Ms);
-      for (int k0 = 0; k0 <= i0; k0 += 16) {  // causal: columns past the row block are zero
-        uint32_t bx[YNT / 2][4];
+          for (int np = 0; np < YNT / 2; ++np) ldsm4_t(b_addr_t(xs_u, XS, p0 + np * 16, k0, lane), bx[np]);
 #pragma unroll
-        for (int np = 0; np < YNT / 2; ++np) ldsm4_t(b_addr_t(xs_u, XS, p0 + np * 16, k0, lane), bx[np]);
+          for (int part = 0; part < 2; ++part) {  // M hi, lo
+            uint32_t a[4];
+            ldsm4(a_addr(ms_u + part * Sm::M_BYTES, MS, i0, k0, lane), a);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {  // M hi, lo
-          uint32_t a[4];
-          ldsm4(a_addr(ms_u + part * Sm::M_BYTES, MS, i0, k0, lane), a);
-#pragma unroll
-          for (int np = 0; np < YNT / 2; ++np) {
-            mma16816(acc[2 * np], a, bx[np][0], bx[np][1]);
-            mma16816(acc[2 * np + 1], a, bx[np][2], bx[np][3]);
+            for (int np = 0; np < YNT / 2; ++np) {
+              mma16816(accd[2 * np], a, bx[np][0], bx[np][1]);
+              mma16816(accd[2 * np + 1], a, bx[np][2], bx[np][3]);
+            }
           }
         }
+        if (k < KQ) {  // B^T Xw over steps k0..k0+15
+          uint32_t a[SMT][4];
+#pragma unroll
+          for (int mt = 0; mt < SMT; ++mt) ldsm4_t(a_addr_t(bs_u, BS, sm0 + mt * 16, k0, lane), a[mt]);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)  // Xw hi, lo
+#pragma unroll
+            for (int np = 0; np < SNT / 2; ++np) {
+              uint32_t bb[4];
+              ldsm4_t(b_addr_t(xw_u + part * Sm::X_BYTES, XS, sn0 + np * 16, k0, lane), bb);
+#pragma unroll
+              for (int mt = 0; mt < SMT; ++mt) {
+                mma16816(sacc[mt][2 * np], a[mt], bb[0], bb[1]);
+                mma16816(sacc[mt][2 * np + 1], a[mt], bb[2], bb[3]);
+              }
+            }
+        }
       }
+      const float e0 = eS[i0 + gq], e1 = eS[i0 + gq + 8];
 #pragma unroll
       for (int nt = 0; nt < YNT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int i = i0 + gq + hh * 8, pp = p0 + nt * 8 + 2 * cq;
+          const float e = hh ? e1 : e0;
           const float2 xv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Xs + i * XS + pp));
           *reinterpret_cast<float2*>(Ys + i * YS + pp) =
-              make_float2(fmaf(Dh, xv.x, acc[nt][2 * hh]), fmaf(Dh, xv.y, acc[nt][2 * hh + 1]));
+              make_float2(fmaf(Dh, xv.x, fmaf(e, acc[nt][2 * hh], accd[nt][2 * hh])),
+                          fmaf(Dh, xv.y, fmaf(e, acc[nt][2 * hh + 1], accd[nt][2 * hh + 1])));
         }
-    }
-    // h_next = exp(S_last) h_prev + B^T Xw
-    {
-      const float dl = eS[Q - 1];
-      const uint32_t xw_u = smem_u32(Xws);
-#pragma unroll
-      for (int mt = 0; mt < SMT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < SNT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] *= dl;
-#pragma unroll
-      for (int k0 = 0; k0 < Q; k0 += 16) {
-        uint32_t a[SMT][4];
-#pragma unroll
-        for (int mt = 0; mt < SMT; ++mt) ldsm4_t(a_addr_t(bs_u, BS, sm0 + mt * 16, k0, lane), a[mt]);
-#pragma unroll
-        for (int part = 0; part < 2; ++part)  // Xw hi, lo
-#pragma unroll
-          for (int np = 0; np < SNT / 2; ++np) {
-            uint32_t bb[4];
-            ldsm4_t(b_addr_t(xw_u + part * Sm::X_BYTES, XS, sn0 + np * 16, k0, lane), bb);
-#pragma unroll
-            for (int mt = 0; mt < SMT; ++mt) {
-              mma16816(sacc[mt][2 * np], a[mt], bb[0], bb[1]);
-              mma16816(sacc[mt][2 * np + 1], a[mt], bb[2], bb[3]);
-            }
-          }
-      }
     }
     __syncthreads();  // every read of this stage, of M, Xw and of the state tile is done
 
