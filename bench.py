@@ -43,10 +43,10 @@ UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDA
 # per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
 # on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (mean of 5 output launches: 256.69 MB read + 58.85 MB write),
+    # long_bf16_16k capture (mean of 5 output launches: 256.68 MB read + 58.83 MB write),
     # scaled by the units processed (x8) to the 131072-step workload
-    "long_bf16": {"bytes_per_launch": 2524000000, "kernel_src_sha": "6a02dbe07c3b7693"},
-    "long_bf16_16k": {"bytes_per_launch": 315540000, "kernel_src_sha": "6a02dbe07c3b7693"},
+    "long_bf16": {"bytes_per_launch": 2524020000, "kernel_src_sha": "ee3f4713096a6f8e"},
+    "long_bf16_16k": {"bytes_per_launch": 315502000, "kernel_src_sha": "ee3f4713096a6f8e"},
 }
 
 
