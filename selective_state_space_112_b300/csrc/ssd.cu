@@ -7,8 +7,8 @@
 // (Y = (L o (Q K^T)) V with a 1-semiseparable decay mask L).
 //
 // One CTA owns one (batch row, head, block of PB channels) and walks its sequence in
-// chunks of Q = 64 steps, carrying that (N, PB) part of the state in fp32 registers.  With S_i the
-// running sum of step * A inside the chunk, for steps i, j of the chunk:
+// chunks of Q = 64 steps, carrying that (N, PB) part of the state in fp32 registers.
+// With S_i the running sum of step * A inside the chunk, for steps i, j of the chunk:
 //   M[i][j]   = (C_i . B_j) exp(S_i - S_j) step_j            j <= i, else 0
 //   y_i       = exp(S_i) C_i . h_prev  +  sum_j M[i][j] x_j  +  D x_i
 //   h_next    = exp(S_last) h_prev  +  sum_j B_j (exp(S_last - S_j) step_j x_j)^T
@@ -57,6 +57,7 @@ struct SsdSmem {
   static constexpr int OFF_S = OFF_Y + Q * YS * 4;       // state hi, state lo
   static constexpr int OFF_V = OFF_S + 2 * S_BYTES;      // per-step vectors, two chunks
   static constexpr int BYTES = OFF_V + 8 * Q * 4;
+  static_assert(BYTES <= 232448, "dynamic shared memory of one CTA");
 };
 
 struct SsdParams {
