@@ -56,6 +56,8 @@ MUTANTS = {
                           "hs[p * N + n] = a * hs[p * N + n] + Bv[n] * xv;"),
     "ssd_readout_before_update": ("          hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;\n          y += Cv[n] * hs[p * N + n];",
                                   "          y += Cv[n] * hs[p * N + n];\n          hs[p * N + n] = a * hs[p * N + n] + step * Bv[n] * xv;"),
+    "ssd_softplus_always": ("const double step = dt_softplus ? oracle_softplus(s) : s;",
+                            "const double step = oracle_softplus(s);"),
     "ssd_skip_dropped": ("y += (D ? D[h] : 0.0) * xv;", "y += 0.0 * xv;"),
     "ssd_state_transposed": ("hs[i] = state_in ? state[(b * H + h) * P * N + i] : 0.0;",
                              "hs[i] = state_in ? state[(b * H + h) * P * N + (i % N) * P + i / N] : 0.0;"),

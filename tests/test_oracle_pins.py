@@ -565,7 +565,7 @@ def _ssd(w, **kw):
     return oracle.ssd(w.x, w.dt, w.A, w.B, w.C, D=w.D, z=w.z, dt_bias=w.dt_bias, h0=w.h0, **kw)
 
 
-def _masked_attention(w, zero_decay=False):
+def _masked_attention(w, zero_decay=False, softplus=True):
     """'Structured State Space Models and Mamba', section 'State Space Duality and
     Mamba-2': Y = (L o (Q K^T)) V with Q = C, K = B, V = step * x and the
     1-semiseparable L[i, j] = exp(A (S_i - S_j)) for j <= i (S = cumulative step
@@ -575,7 +575,7 @@ def _masked_attention(w, zero_decay=False):
     batch, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     v = dtr + (0.0 if bias is None else bias)
-    step = np.logaddexp(0.0, v)                                   # softplus, (b, L, H)
+    step = np.logaddexp(0.0, v) if softplus else v                # softplus, (b, L, H)
     out = np.empty_like(x)
     fin = np.empty((batch, H, P, N))
     for b in range(batch):
@@ -631,6 +631,19 @@ def test_ssd_is_the_selective_scan_with_a_tied_decay():
             h0=h0[:, heads].reshape(batch, -1, N))
         np.testing.assert_allclose(out[:, :, heads].reshape(batch, L, -1), o1, rtol=1e-13, atol=1e-14)
         np.testing.assert_allclose(st[:, heads].reshape(batch, -1, N), s1, rtol=1e-13, atol=1e-14)
+
+
+def test_ssd_step_without_softplus():
+    """With dt_softplus off the step is dt + dt_bias as given (small positive raw
+    steps here), in the masked-attention form as well."""
+    w = _ssd_case(38, state_in=True)
+    raw = np.abs(np.random.default_rng(38).standard_normal(w.dt.shape)).astype(np.float32) * 0.1
+    w.dt = f32_to_bf16_bits(raw)
+    w.dt_bias = np.full(w.nheads, 0.01, np.float32)
+    out, st = _ssd(w, dt_softplus=False)
+    ref, ref_st = _masked_attention(w, softplus=False)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(st, ref_st, rtol=1e-11, atol=1e-12)
 
 
 def test_ssd_zero_decay_is_causal_linear_attention():
