@@ -29,7 +29,9 @@
  *  - Return value: SSM_OK (0) or a negative ssm_status; argument errors are
  *    detected on the host before anything is enqueued.
  *  - No CPU fallback: without a usable GPU every call fails with SSM_ERR_CUDA.
- *  - Deterministic: identical inputs give bitwise-identical outputs.
+ *  - The forward entry points are deterministic: identical inputs give
+ *    bitwise-identical outputs.  The backward pass is not: its sums over
+ *    channels use fp32 atomic additions, whose rounding order varies.
  */
 #ifndef SSM_SCAN_H
 #define SSM_SCAN_H

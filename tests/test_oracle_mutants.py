@@ -1,8 +1,10 @@
-"""The pins must catch plausible mistakes in the oracle.
+"""The pins must catch plausible mistakes in the oracle and in the parity checker.
 
 Each case plants one mistake (a dropped term, a wrong sign, index or operand)
 in a copy of oracle/ssm_oracle.c, compiles it on the CPU, and runs the pin
-suite against it in a child process; the pins must fail.
+suite against it in a child process; the pins must fail.  The same is done for
+the error metric every parity test uses (oracle/metrics.py) against its
+hand-computed pins.
 """
 import os
 import subprocess
@@ -81,3 +83,37 @@ def test_pins_catch_mutant(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# Planted mistakes in the parity checker (oracle/metrics.py); its hand-computed pins
+# (tests/test_metrics_pins.py) must fail for each.
+METRICS_SRC = os.path.join(ROOT, "oracle", "metrics.py")
+METRIC_MUTANTS = {
+    "mean_for_max": ("return float(np.max(np.abs(g - r) / den))", "return float(np.mean(np.abs(g - r) / den))"),
+    "floor_at_max": ("fl = rms(r) if floor is None else float(floor)",
+                     "fl = float(np.max(np.abs(r))) if floor is None else float(floor)"),
+    "floor_at_mean_abs": ("fl = rms(r) if floor is None else float(floor)",
+                          "fl = float(np.mean(np.abs(r))) if floor is None else float(floor)"),
+    "rms_without_sqrt": ("return float(np.sqrt(np.mean(r * r))) if r.size else 0.0",
+                         "return float(np.mean(r * r)) if r.size else 0.0"),
+    "no_floor": ("den = np.maximum(np.abs(r), fl)", "den = np.abs(r)"),
+    "signed_reference": ("den = np.maximum(np.abs(r), fl)", "den = np.maximum(r, fl)"),
+    "signed_difference": ("return float(np.max(np.abs(g - r) / den))", "return float(np.max((g - r) / den))"),
+    "finite_guard_dropped": ("    if not np.all(np.isfinite(g)):\n        return float(\"inf\")\n", ""),
+    "report_unfloored_all_entries": ("\"max_rel_unfloored\": float((d[nz] / np.abs(r[nz])).max()) if nz.any() else 0.0,",
+                                     "\"max_rel_unfloored\": float((d[nz] / np.abs(r[nz])).mean()) if nz.any() else 0.0,"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(METRIC_MUTANTS))
+def test_metric_pins_catch_mutant(name, tmp_path):
+    orig, mutated = METRIC_MUTANTS[name]
+    src = open(METRICS_SRC).read()
+    assert src.count(orig) == 1, f"mutation site for {name} not found exactly once"
+    mpath = tmp_path / "metrics_mutant.py"
+    mpath.write_text(src.replace(orig, mutated))
+    env = dict(os.environ, SSM_METRICS_PATH=str(mpath))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_metrics_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"metric pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
