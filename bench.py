@@ -39,14 +39,14 @@ FMA_LANES_PER_SM_CLK = 128
 FMA_OPS_PER_UPDATE = 4
 UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDATE)
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the output-pass kernel
-# per launch, from one ncu capture, with the sha256 of the kernel sources it was taken
-# on; reported as null once the sources change.  See profiles/.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one whole call (all of
+# its kernel launches), from one ncu capture, with the sha256 of the kernel sources it
+# was taken on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (mean of 5 output launches: 256.68 MB read + 58.83 MB write),
-    # scaled by the units processed (x8) to the 131072-step workload
-    "long_bf16": {"bytes_per_launch": 2524020000, "kernel_src_sha": "ee3f4713096a6f8e"},
-    "long_bf16_16k": {"bytes_per_launch": 315502000, "kernel_src_sha": "ee3f4713096a6f8e"},
+    # long_bf16_16k capture (aggregate launch 167.4 MB + output launch 315.5 MB, means
+    # of 5), scaled by the units processed (x8) to the 131072-step workload
+    "long_bf16": {"bytes_per_call": 3863000000, "kernel_src_sha": "ee3f4713096a6f8e"},
+    "long_bf16_16k": {"bytes_per_call": 482900000, "kernel_src_sha": "ee3f4713096a6f8e"},
 }
 
 
@@ -206,21 +206,28 @@ def oracle_sample(w, k, cv=None):
     return time.perf_counter() - t
 
 
-def cpu_baseline(w, budget_s: float = 15.0, cv=None):
+# One sample rule for the CPU baseline and the reference arm: channels 0..k-1 of
+# batch row 0 over the whole sequence, k = min(dim, CPU_SAMPLE_CHANNELS), with the
+# sample's inputs sliced before the timed region.  At 512 channels the fixed cost of
+# a call (widening B and C of the whole sequence) is a few percent of its time.
+CPU_SAMPLE_CHANNELS = 512
+
+
+def cpu_sample_channels(w) -> int:
+    return min(w.dim, CPU_SAMPLE_CHANNELS)
+
+
+def cpu_baseline(w, cv=None):
     import oracle
     cores = oracle.max_threads()
-    cap = min(w.dim, 512)
-    k = min(cap, max(cores, 8))
+    k = cpu_sample_channels(w)
+    oracle_sample(w, min(k, cores), cv)  # loads the library, starts the thread pool
     t = oracle_sample(w, k, cv)
-    k2 = int(min(cap, max(k, k * budget_s / max(t, 1e-3))))
-    k2 = max(1, (k2 // cores) * cores) if k2 >= cores else k2
-    if k2 > k:
-        t, k = oracle_sample(w, k2, cv), k2
     units = k * w.seqlen
     what = "block prologue + scan" if cv is not None else "scan"
     return {"value": units / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, N={w.dstate}, {what} "
-                      f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
+                      f"({units} tokens*channels, {t:.2f} s, float64 C + OpenMP)"}
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -236,6 +243,136 @@ def job_throughput(units_per_rank: int, steps: int, ms_max: float, world: int) -
     return world * units_per_rank * steps / (ms_max * 1e-3)
 
 
+def whole_call_traffic(workload: str, conv: bool):
+    """DRAM bytes (read + write) of one whole call from the recorded ncu capture, or
+    None when none is recorded for the current kernel sources."""
+    tr = TRAFFIC.get(workload)
+    if tr and not conv and tr["kernel_src_sha"] == kernel_src_sha():
+        return tr["bytes_per_call"]
+    return None
+
+
+def roofline(w, ms_call, prof, torch, device, clocks, traffic=None):
+    """HBM roofline of one call (all of its kernels) and the arithmetic bound beside it.
+
+    achieved = algorithmic bytes of the call / device time of the call; peak = the
+    measured copy bandwidth.  The arithmetic bound counts one MUFU ex2 per state update
+    at 32 per SM per clock, at the median SM clock sampled while timing."""
+    hbm_peak, sm_max, peak_kind = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    alg = w.algorithmic_bytes()
+    achieved = alg / (ms_call * 1e-3) / 1e9
+    mhz = clocks.get("sm_mhz") or sm_max
+    upd_peak = UPDATES_PER_SM_CLK * sms * mhz * 1e6 / 1e9           # Gupdate/s
+    upd_achieved = w.element_updates / (ms_call * 1e-3) / 1e9
+    total_ms = sum(v[1] for v in prof.values()) or 1.0
+    return {"bound": "hbm", "kernel": "whole call (" + ", ".join(sorted(prof)) + ")",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_source": peak_kind,
+            "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+            "kernel_ms_avg": round(ms_call, 4),
+            "alu": {"achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
+                    "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
+                    "peak_basis": (f"min({EX2_PER_SM_CLK} MUFU ex2, {FMA_LANES_PER_SM_CLK}/"
+                                   f"{FMA_OPS_PER_UPDATE} FMA lanes) state updates per SM per clock"
+                                   f" (measured on B300) x {sms} SMs x {mhz:.0f} MHz (median sampled)")},
+            "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4),
+                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()}}
+
+
+def timed_calls(fn, torch, stream, reps, flush=None):
+    """Device times (ms) of `reps` calls of fn, each bracketed by CUDA events on the
+    launch stream; flush() (an L2-sized write) runs between calls, outside the events.
+    A short device-side wait before the first event lets the host enqueue the call
+    while the GPU is still busy, so that the host's launch cost stays outside."""
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        torch.cuda._sleep(400000)  # about 0.2 ms of device time
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def other_workloads(torch, ssm, device, names, reps=20):
+    """The other scan workloads, timed in the same run: per call the median, min and
+    90th percentile of `reps` calls with the L2 flushed between them, the HBM and
+    arithmetic fractions, and the per-kernel split.  The recurrent-step workload is
+    also timed as 128 chained steps in one CUDA graph (its state stays in L2 across
+    steps, as in decoding)."""
+    from selective_state_space_112_b300.workloads import config
+    stream = torch.cuda.current_stream(device)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush = lambda: flush_buf.zero_()
+    out = {}
+    for name in names:
+        w = config(name)
+        t = device_tensors(w, torch, device)
+        o = torch.empty_like(t["x"])
+        state_in = w.h0 is not None
+        fs = t["h0"].clone() if state_in else torch.empty((w.batch, w.dim, w.dstate),
+                                                           dtype=torch.float32, device=device)
+
+        def call():
+            ssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                       t["delta_bias"], out=o, final_state=fs,
+                                       delta_softplus=w.delta_softplus, state_in=state_in)
+        for _ in range(3):
+            call()
+        assert ssm.ssm_check_status() == 0
+        ssm.ssm_profile_enable(True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            times = timed_calls(call, torch, stream, reps, flush)
+        ssm.ssm_profile_enable(False)
+        prof = ssm.ssm_profile_read()
+        assert ssm.ssm_check_status() == 0
+        times.sort()
+        med = statistics.median(times)
+        latency = w.algorithmic_bytes() < 126e6 and name != "step_bf16"
+        rf = roofline(w, med, prof, torch, device, clk.summary())
+        rec = {"shape": {"batch": w.batch, "seqlen": w.seqlen, "dim": w.dim, "dstate": w.dstate,
+                         "io_dtype": w.io, "gate": w.z is not None, "state_in": state_in},
+               "ms_median": round(med, 5), "ms_min": round(times[0], 5),
+               "ms_p90": round(times[int(0.9 * (len(times) - 1))], 5),
+               "tokens_channels_per_s": w.tokens_channels / (med * 1e-3),
+               "reps": reps, "l2": "flushed between calls (256 MB write)",
+               "roofline": None if latency else {k: rf[k] for k in ("bound", "achieved", "peak",
+                                                                   "unit", "frac", "alu")},
+               "kernels": rf["kernels"], "clocks": clk.summary()}
+        if latency:
+            rec["note"] = "inputs fit in L2: a latency figure, no roofline claim"
+        if name == "step_bf16":
+            # 128 recurrent steps chained in one CUDA graph, each advancing the state
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    call()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                for _ in range(128):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            gt = timed_calls(g.replay, torch, stream, 10)
+            gm = statistics.median(gt) / 128
+            rec["graph_chain"] = {"steps": 128, "ms_per_step": round(gm, 5),
+                                  "hbm_gbs": round(w.algorithmic_bytes() / (gm * 1e-3) / 1e9, 1),
+                                  "l2": "state carried in L2 across the chained steps"}
+            del g
+        out[name] = rec
+        del t, o, fs
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -246,6 +383,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads (the line's `configs` object)")
     ap.add_argument("--conv", action="store_true",
                     help="the Mamba-block prologue (causal conv of width 4 + silu) fused in")
     ap.add_argument("--backward", action="store_true",
@@ -346,30 +485,12 @@ def main():
     units = w.tokens_channels
     value = job_throughput(units, args.steps, ms, world)
 
-    # ---- roofline of the dominant kernel (CUDA events recorded around each launch)
-    hbm_peak, sm_max, peak_kind = load_peaks()
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    alg = w.algorithmic_bytes()
-    dom = max(prof, key=lambda k: prof[k][1]) if prof else None
-    dom_ms = prof[dom][1] / prof[dom][0] if dom else ms_step
-    total_ms = sum(v[1] for v in prof.values()) or 1.0
-    hbm_achieved = alg / (dom_ms * 1e-3) / 1e9                      # GB/s
-    upd_peak = UPDATES_PER_SM_CLK * sms * sm_max * 1e6 / 1e9           # Gupdate/s
-    upd_achieved = w.element_updates / (dom_ms * 1e-3) / 1e9
-    tr = TRAFFIC.get(args.workload)
-    traffic = (tr["bytes_per_launch"] if tr and dom == "ssm_scan_output" and not args.conv
-               and tr["kernel_src_sha"] == kernel_src_sha() else None)
-    roof = {"bound": "alu", "kernel": dom, "achieved": round(upd_achieved, 1), "peak": round(upd_peak, 1),
-            "unit": "Gupdate/s", "frac": round(upd_achieved / upd_peak, 4),
-            "peak_basis": (f"min({EX2_PER_SM_CLK} MUFU ex2, {FMA_LANES_PER_SM_CLK}/{FMA_OPS_PER_UPDATE} FMA lanes)"
-                           f" state updates per SM per clock (measured on B300) x {sms} SMs x"
-                           f" {sm_max:.0f} MHz"),
-            "traffic": traffic, "algorithmic_bytes_per_launch": alg,
-            "kernel_ms_avg": round(dom_ms, 4),
-            "hbm": {"achieved": round(hbm_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(hbm_achieved / hbm_peak, 4), "peak_source": peak_kind},
-            "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4),
-                            "share": round(v[1] / total_ms, 4)} for k, v in prof.items()}}
+    # ---- roofline: the whole call against HBM (the path's stated roofline: the
+    # minimum bytes in and out over the copy bandwidth), with the arithmetic bound
+    # beside it at the SM clock sampled during the timed region
+    clocks = clk.summary()
+    roof = roofline(w, ms_step, prof, torch, device, clocks,
+                    traffic=whole_call_traffic(args.workload, args.conv))
 
     res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -380,10 +501,9 @@ def main():
                       "gate": w.z is not None, "state_in": state_in,
                       "prologue": "causal conv width 4 + silu" if args.conv else "none",
                       "parallelism": f"replica x{world}" if world > 1 else "single",
-                      "l2": f"inputs {alg / 1e9:.2f} GB > 126 MB L2; no flush needed"
-                            if alg > 4 * 126e6 else "L2 resident (latency case)"},
-           "hbm_gbs_step": round(alg / (ms_step * 1e-3) / 1e9, 1),
-           "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary()}
+                      "l2": f"inputs {w.algorithmic_bytes() / 1e9:.2f} GB > 126 MB L2; no flush needed"
+                            if w.algorithmic_bytes() > 4 * 126e6 else "L2 resident (latency case)"},
+           "roofline": roof, "gpu_launches": int(launches), "clocks": clocks}
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
@@ -428,6 +548,10 @@ def main():
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": ems / args.e2e_steps}
 
+    if rank == 0 and world == 1 and not args.no_configs and not args.conv:
+        others = [n for n in ("mamba130m_f32", "mamba1p4b_bf16", "step_bf16", "lti_f32", "tiny_f32")
+                  if n != args.workload]
+        res["configs"] = other_workloads(torch, ssm, device, others)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, cv=cv)
     if world > 1:
@@ -783,8 +907,14 @@ def reference_arm(args, world, rank):
     import oracle
     w = config(args.workload)
     cores = oracle.max_threads()
-    k = min(w.dim, max(cores, 8))
-    for _ in range(min(args.warmup, 1)):
+    k = cpu_sample_channels(w)
+    oracle_sample(w, min(k, cores))  # loads the library, starts the thread pool
+    t1 = oracle_sample(w, k)
+    budget = 240.0  # seconds for all warm-up and timed steps
+    if (args.steps + args.warmup) * t1 > budget:
+        # the same rule on fewer channels, so that the run ends within minutes
+        k = max(min(k, cores), int(k * budget / ((args.steps + args.warmup) * t1)))
+    for _ in range(max(args.warmup - 1, 0)):
         oracle_sample(w, k)
     el = 0.0
     for _ in range(args.steps):
@@ -798,10 +928,10 @@ def reference_arm(args, world, rank):
            "config": {"workload": args.workload, "batch": w.batch, "seqlen": w.seqlen,
                       "dim": w.dim, "dstate": w.dstate, "io_dtype": w.io},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps per step"},
+                            "sample": f"channels 0..{k - 1} of batch row 0, all {w.seqlen} steps, "
+                                      f"N={w.dstate}, per step (the CPU baseline's sample rule)"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
-
 
 
 def reference_arm_ssd(args, world):

@@ -196,16 +196,19 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A,
  * errors are those of ssm_selective_scan_fwd, with these differences:
  *  - The chunk-carry workspace lives in one fixed device array of
  *    SSM_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that loads it
- *    until the process exits.  A call whose workspace would be larger (long sequences
- *    with many chunks: (chunks - 1) * batch * dim * (dstate + 1) * 4 bytes, plus
- *    batch * dim * dstate * 4 with state_in) returns SSM_ERR_SCRATCH and launches
- *    nothing.  Calls that need no chunking use no workspace.
+ *    until the process exits.  When the automatic chunk count would need more (long
+ *    sequences with many chunks: about (chunks - 1) * batch * dim * (2 dstate + 1) * 4
+ *    bytes, plus batch * dim * dstate * 4 with state_in), the call uses fewer chunks,
+ *    down to one (no workspace).  A chunk count forced with ssm_set_option("chunks")
+ *    whose workspace does not fit returns SSM_ERR_SCRATCH and launches nothing.
  *  - The first call on a device asks the runtime for the array's address (once per
  *    device, with that device current); make that first call before any stream
  *    capture.
  *  - All calls on a device share the array and the array keeps the last call's
- *    contents (nothing in it must start at zero).  Calls that may overlap on the GPU
- *    (different streams without ordering) race on it: order them on one stream.
+ *    contents; each call clears the part that must start at zero (its chunk-carry
+ *    flags) with a cudaMemsetAsync on `stream` before its kernel.  Calls that may
+ *    overlap on the GPU (different streams without ordering) race on it: order them
+ *    on one stream.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 int ssm_selective_scan_fwd_noalloc(const void* x, const void* delta, const float* A,
@@ -231,6 +234,11 @@ const char* ssm_status_string(int code);
  * padded dstate * 4 bytes, 5.4 GB for a 131072-step, 2560-channel layer) this
  * gives that memory back. */
 int ssm_release_workspace(void);
+
+/* Device memory the library's pool holds on the current device (bytes reserved from
+ * the driver, in use or kept for reuse; 0 before the first pooled call), or a
+ * negative ssm_status. */
+int64_t ssm_workspace_reserved_bytes(void);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t ssm_kernel_launches(void);

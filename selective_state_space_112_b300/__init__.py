@@ -14,7 +14,8 @@ from ._abi import (SSM_BC_PER_CHANNEL, SSM_BC_TIME_VARYING, SSM_BF16, SSM_F32, S
 __all__ = ["ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_bwd",
            "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
-           "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
+           "ssm_release_workspace", "ssm_workspace_reserved_bytes", "ssm_kernel_launches",
+           "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read", "ssm_ssd_fwd", "SSMError", "SsmDims",
            "SsdDims"]
 
@@ -268,6 +269,7 @@ def ssm_check_status(stream=None) -> int:
 
 ssm_status_string = _abi.status_string
 ssm_release_workspace = _abi.release_workspace
+ssm_workspace_reserved_bytes = _abi.workspace_reserved_bytes
 ssm_kernel_launches = _abi.kernel_launches
 ssm_set_option = _abi.set_option
 ssm_profile_enable = _abi.profile_enable

@@ -28,7 +28,7 @@ SSM_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/ssm_scan.h
 EXPORTS = ("ssm_selective_scan_fwd", "ssm_conv_selective_scan_fwd", "ssm_selective_scan_bwd",
            "ssm_selective_scan_fwd_noalloc",
            "ssm_check_status", "ssm_status_string",
-           "ssm_release_workspace", "ssm_kernel_launches", "ssm_set_option",
+           "ssm_release_workspace", "ssm_workspace_reserved_bytes", "ssm_kernel_launches", "ssm_set_option",
            "ssm_profile_enable", "ssm_profile_read",
            # include/ssm_ssd.h
            "ssm_ssd_fwd")
@@ -91,6 +91,8 @@ def lib():
             L.ssm_status_string.argtypes = [i32]
             L.ssm_release_workspace.restype = i32
             L.ssm_release_workspace.argtypes = []
+            L.ssm_workspace_reserved_bytes.restype = i64
+            L.ssm_workspace_reserved_bytes.argtypes = []
             L.ssm_kernel_launches.restype = ctypes.c_uint64
             L.ssm_kernel_launches.argtypes = []
             L.ssm_set_option.restype = i32
@@ -148,6 +150,13 @@ def check_status(stream=0) -> int:
 
 def release_workspace() -> int:
     return lib().ssm_release_workspace()
+
+
+def workspace_reserved_bytes() -> int:
+    n = int(lib().ssm_workspace_reserved_bytes())
+    if n < 0:
+        raise SSMError(n, "ssm_workspace_reserved_bytes")
+    return n
 
 
 def kernel_launches() -> int:

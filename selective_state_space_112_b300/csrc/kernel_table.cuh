@@ -4,6 +4,7 @@
 // (kernels_<io>_<layout>[_zoh|_conv].cu) so that they build in parallel.
 #pragma once
 
+#include "scan_fused.cuh"
 #include "scan_tile.cuh"
 
 namespace ssm {
@@ -61,6 +62,22 @@ KernelInfo lookup_bf16_tv_zoh(int S, int G, int pass);
 KernelInfo lookup_bf16_lti_zoh(int S, int G, int pass);
 KernelInfo lookup_f32_tv_conv(int S, int G, int pass);
 KernelInfo lookup_bf16_tv_conv(int S, int G, int pass);
+
+// Two-channel kernel with the chunk carry in one launch (scan_fused.cuh), built for
+// time-varying B and C, the fused scan's input term and S = N in {4, 8, 16} (bf16:
+// {8, 16}); kernels_fused.cu.
+typedef void (*FusedFn)(TmaMaps, FusedParams);
+
+struct FusedInfo {
+  FusedFn fn = nullptr;
+  int nt = 0;    // threads per CTA
+  int ch = 0;    // channels per CTA
+  int cw = 0;    // channels per consumer warp
+  int t = 0;     // steps per tile
+  int smem = 0;  // dynamic shared memory bytes
+};
+
+FusedInfo lookup_fused(int io_bf16, int S);
 
 // Recurrent step kernel (sequence length 1), step_kernel.cu: G threads per channel of
 // 4 states each, G in {1, 2, 4, 8, 16}.

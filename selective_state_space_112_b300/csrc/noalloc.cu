@@ -50,8 +50,9 @@ extern "C" int ssm_selective_scan_fwd_noalloc(const void* x, const void* delta, 
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != SSM_OK) return rc;
-  // Nothing in the scratch has to start at zero: the aggregate pass writes every entry
-  // that the output pass of the same call reads.
+  // The call clears the scratch's chunk-carry flags itself (in stream order) before its
+  // kernel; everything else a kernel reads from the scratch was written earlier in the
+  // same call.
   return ssm_internal::scan_forward(x, delta, A, B, C, D, z, delta_bias, out, final_state, dims, stream,
                                     scratch, SSM_NOALLOC_SCRATCH_BYTES, nullptr);
 }

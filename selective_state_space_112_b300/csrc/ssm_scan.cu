@@ -33,6 +33,8 @@ std::atomic<int64_t> g_opt_ctas_per_sm{3};
 std::atomic<int64_t> g_opt_pow_path{1};
 std::atomic<int64_t> g_opt_tma{1};
 std::atomic<int64_t> g_opt_inject_stall{0};  // tests: 1 + tile index the producer withholds
+std::atomic<int64_t> g_opt_fused{1};         // two-channel kernel with the carry in one launch
+std::atomic<int64_t> g_opt_hold_chunk{0};    // tests: 1 + chunk index that never publishes
 std::atomic<uint64_t> g_launches{0};
 
 __device__ int g_status;  // raised by a kernel: kStatusTimeout, or any other nonzero value
@@ -46,9 +48,9 @@ struct ProfRec {
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof;
-constexpr int kKinds = 5;
+constexpr int kKinds = 6;
 const char* const kKindName[kKinds] = {"ssm_chunk_aggregate", "ssm_scan_output", "ssm_step",
-                                      "ssm_bwd_reverse_aggregate", "ssm_bwd_main"};
+                                      "ssm_bwd_reverse_aggregate", "ssm_bwd_main", "ssm_scan_fused"};
 
 // ------------------------------------------------------- per-device pools
 
@@ -157,11 +159,22 @@ int occupancy(const ssm::KernelInfo& k) {
 // Lanes per channel: the fewest (least per-state overhead) that give at least
 // `lane_threads` threads over the batch rows and channels; one otherwise (the
 // sequence is then chunked).
+// Workspace of the two-kernel chunk carry with k chunks: end states and step sums of
+// chunks 0 .. k-2, a copy of the initial state and of the prologue's input history.
+size_t chunk_ws_bytes(const ssm_dims& d, int64_t k, bool conv) {
+  if (k <= 1) return 0;
+  const size_t nH = (size_t)(k - 1) * d.batch * d.dim * d.dstate;
+  const size_t nS = (size_t)(k - 1) * d.batch * d.dim;
+  const size_t nh0 = d.state_in ? (size_t)d.batch * d.dim * d.dstate : 0;
+  const size_t ncs = (conv && d.state_in) ? (size_t)d.batch * d.dim * 3 : 0;
+  return (nH + nS + nh0 + ncs) * sizeof(float);
+}
+
 // Chunks along the sequence only when that leaves fewer than `ctas_per_sm` CTAs per
 // SM: every chunk but the last is then scanned twice (aggregate, output), so the
 // chunk count is the largest that still fits ctas_per_sm CTAs on every SM (one
 // wave, evenly spread).
-bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl) {
+bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl, size_t max_ws_bytes) {
   const int ns = padded_states(d.dstate);
   const bool lti = d.bc_layout == SSM_BC_PER_CHANNEL;
   std::vector<int> cand;
@@ -209,10 +222,17 @@ bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl) {
   k = std::max<int64_t>(1, std::min<int64_t>(k, (d.seqlen + ssm::kChunkAlign - 1) / ssm::kChunkAlign));
   k = std::min<int64_t>(k, 65535);
   // chunk length: a multiple of kChunkAlign steps, so tiles never straddle chunks
-  int64_t len = (d.seqlen + k - 1) / k;
-  len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
-  pl->chunk_len = std::max<int64_t>(len, ssm::kChunkAlign);
-  pl->nchunks = (int)((d.seqlen + pl->chunk_len - 1) / pl->chunk_len);
+  auto split = [&](int64_t kk) {
+    int64_t len = (d.seqlen + kk - 1) / kk;
+    len = ((len + ssm::kChunkAlign - 1) / ssm::kChunkAlign) * ssm::kChunkAlign;
+    pl->chunk_len = std::max<int64_t>(len, ssm::kChunkAlign);
+    pl->nchunks = (int)((d.seqlen + pl->chunk_len - 1) / pl->chunk_len);
+  };
+  split(k);
+  if (max_ws_bytes && g_opt_chunks.load() <= 0) {
+    // a fixed scratch: fewer automatic chunks until the workspace fits
+    while (pl->nchunks > 1 && chunk_ws_bytes(d, pl->nchunks, conv) > max_ws_bytes) split(pl->nchunks - 1);
+  }
   return true;
 }
 
@@ -296,10 +316,198 @@ int launch_bwd(ssm::BwdFn fn, int kind, dim3 grid, const ssm::BwdParams& p, cuda
   return SSM_OK;
 }
 
+// ------------------------------------------------- two-channel fused kernel
+
+// The fused kernel serves time-varying B and C, the fused scan's input term, no
+// prologue, shapes a tensor map can describe, and N in {4, 8, 16} (bf16: 8, 16).
+ssm::FusedInfo fused_kernel_for(const ssm_dims& d, bool conv) {
+  if (!g_opt_fused.load() || conv || d.bbar_mode != 0 || d.bc_layout != SSM_BC_TIME_VARYING ||
+      !g_opt_tma.load() || !tma_ok(d) || (g_opt_lanes.load() > 1))
+    return ssm::FusedInfo();
+  if (d.dstate != 4 && d.dstate != 8 && d.dstate != 16) return ssm::FusedInfo();
+  return ssm::lookup_fused(d.io_dtype == SSM_BF16, (int)d.dstate);
+}
+
+bool prepare_fused(const ssm::FusedInfo& k) {
+  static std::mutex mu;
+  static std::vector<const void*> done;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto f : done)
+    if (f == (const void*)k.fn) return true;
+  if (cudaFuncSetAttribute((const void*)k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
+      cudaSuccess)
+    return false;
+  done.push_back((const void*)k.fn);
+  return true;
+}
+
+int fused_occupancy(const ssm::FusedInfo& k) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& e : cache)
+      if (e.first == (const void*)k.fn) return e.second;
+  }
+  int occ = 0;
+  if (!prepare_fused(k) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)k.fn, k.nt, k.smem) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  std::lock_guard<std::mutex> lk(mu);
+  cache.push_back({(const void*)k.fn, occ});
+  return occ;
+}
+
+// Longest chunk: a chunk's first scan is the longest time a CTA waits for another
+// (every wait of the kernels gives up after 2 s), so chunks stay short enough.
+constexpr int64_t kMaxChunkLen = 1 << 18;
+
+// Workspace of the fused kernel with k chunks: flags and the ticket counter (zeroed
+// before every launch), then the step sums, aggregates and prefixes of chunks
+// 0 .. k-2, then a copy of the initial state.
+struct FusedWs {
+  size_t flag_bytes = 0, bytes = 0;
+  size_t off_S = 0, off_H = 0, off_P = 0, off_h0 = 0;
+};
+
+FusedWs fused_ws(const ssm_dims& d, int64_t k, int nwb) {
+  FusedWs w;
+  if (k <= 1) return w;
+  const size_t nflags = (size_t)(k - 1) * d.batch * nwb + 1;
+  w.flag_bytes = (nflags * 4 + 255) / 256 * 256;
+  const size_t nS = (size_t)(k - 1) * d.batch * d.dim;
+  const size_t nH = nS * d.dstate;
+  w.off_S = w.flag_bytes;
+  w.off_H = w.off_S + (nS * 4 + 255) / 256 * 256;
+  w.off_P = w.off_H + nH * 4;
+  w.off_h0 = w.off_P + nH * 4;
+  w.bytes = w.off_h0 + (d.state_in ? (size_t)d.batch * d.dim * d.dstate * 4 : 0);
+  return w;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + nb && y < x + na;
+}
+
+// One call on the fused kernel (see scan_fused.cuh): plan the chunks, take the
+// workspace, clear its flags, encode the tensor maps, launch once.
+int run_fused(const ssm::FusedInfo& fk, const ssm_dims& d, int sms, int dev, const void* x,
+              const void* delta, const float* A, const void* B, const void* C, const float* D,
+              const void* z, const float* delta_bias, void* out, float* final_state,
+              cudaStream_t stream, void* scratch, size_t scratch_bytes) {
+  if (!prepare_fused(fk)) return SSM_ERR_CUDA;
+  const int ncb = (int)((d.dim + fk.ch - 1) / fk.ch);
+  const int nwb = ncb * (fk.ch / fk.cw);
+  const int64_t per_chunk = d.batch * ncb;
+  const int64_t max_chunks = (d.seqlen + ssm::kChunkAlign - 1) / ssm::kChunkAlign;
+  int64_t k = g_opt_chunks.load();
+  const bool forced = k > 0;
+  if (!forced) {
+    // as many chunks as fill every SM with the kernel's resident CTAs in one wave
+    const int64_t slots = (int64_t)sms * fused_occupancy(fk);
+    k = per_chunk >= slots ? 1 : slots / per_chunk;
+    const int64_t min_len = std::max<int64_t>(ssm::kChunkAlign, g_opt_min_chunk_len.load());
+    k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / min_len));
+  }
+  k = std::max<int64_t>(k, (d.seqlen + kMaxChunkLen - 1) / kMaxChunkLen);
+  k = std::max<int64_t>(1, std::min<int64_t>(k, max_chunks));
+  auto split = [&](int64_t kk, int64_t* len, int* nch) {
+    int64_t l = (d.seqlen + kk - 1) / kk;
+    l = (l + ssm::kChunkAlign - 1) / ssm::kChunkAlign * ssm::kChunkAlign;
+    *len = l;
+    *nch = (int)((d.seqlen + l - 1) / l);
+  };
+  int64_t len = 0;
+  int nch = 1;
+  split(k, &len, &nch);
+  if (scratch) {
+    // the fixed scratch: fewer chunks until the workspace fits (a forced count does not shrink)
+    while (nch > 1 && fused_ws(d, nch, nwb).bytes > scratch_bytes) {
+      if (forced || len >= kMaxChunkLen) return SSM_ERR_SCRATCH;
+      split(nch - 1, &len, &nch);
+    }
+  }
+  if ((int64_t)nch * per_chunk > INT32_MAX) return SSM_ERR_DIMS;
+
+  ssm::FusedParams p;
+  std::memset(&p, 0, sizeof p);
+  p.x = x; p.delta = delta; p.z = z; p.out = out; p.A = A; p.B = B; p.C = C;
+  p.Dskip = D; p.bias = delta_bias; p.final_state = final_state;
+  p.h_init = d.state_in ? final_state : nullptr;
+  p.batch = d.batch; p.seqlen = d.seqlen; p.dim = d.dim; p.dstate = (int)d.dstate;
+  p.nchunks = nch; p.chunk_len = len; p.ncb = ncb; p.nwb = nwb;
+  p.delta_softplus = d.delta_softplus;
+  p.pow_path = (int)g_opt_pow_path.load();
+  p.stall_tile = (int)g_opt_inject_stall.load() - 1;
+  p.hold_chunk = (int)g_opt_hold_chunk.load() - 1;
+  int* status = nullptr;
+  if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
+  p.status = status;
+
+  const size_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
+  const int eb = (int)esz;
+  ssm::TmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  bool okm = encode3d(&maps.x, x, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
+             encode3d(&maps.delta, delta, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
+             encode3d(&maps.out, out, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
+             encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, fk.t) &&
+             encode3d(&maps.C, C, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, fk.t);
+  if (okm && z) okm = encode3d(&maps.z, z, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t);
+  if (!okm) return SSM_ERR_CUDA;
+
+  void* ws = nullptr;
+  if (nch > 1) {
+    const FusedWs w = fused_ws(d, nch, nwb);
+    unsigned char* base = nullptr;
+    if (scratch) {
+      base = static_cast<unsigned char*>(scratch);
+    } else {
+      cudaMemPool_t pool;
+      if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+      if (cudaMallocFromPoolAsync(&ws, w.bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+      base = static_cast<unsigned char*>(ws);
+    }
+    p.flags = reinterpret_cast<unsigned*>(base);
+    p.ticket = p.flags + (size_t)(nch - 1) * d.batch * nwb;
+    p.agg_S = reinterpret_cast<float*>(base + w.off_S);
+    p.agg_H = reinterpret_cast<float*>(base + w.off_H);
+    p.pre_H = reinterpret_cast<float*>(base + w.off_P);
+    p.ws_h0 = d.state_in ? reinterpret_cast<float*>(base + w.off_h0) : nullptr;
+    if (cudaMemsetAsync(base, 0, w.flag_bytes, stream) != cudaSuccess) {
+      if (ws) cudaFreeAsync(ws, stream);
+      return SSM_ERR_CUDA;
+    }
+  }
+
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  int rc = SSM_OK;
+  if (prof && (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
+               cudaEventRecord(e0, stream) != cudaSuccess))
+    rc = SSM_ERR_CUDA;
+  if (rc == SSM_OK) {
+    fk.fn<<<dim3((unsigned)(nch * per_chunk)), fk.nt, fk.smem, stream>>>(maps, p);
+    if (cudaGetLastError() != cudaSuccess) rc = SSM_ERR_CUDA;
+    else g_launches.fetch_add(1);
+  }
+  if (rc == SSM_OK && prof) {
+    if (cudaEventRecord(e1, stream) != cudaSuccess) {
+      rc = SSM_ERR_CUDA;
+    } else {
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      g_prof.push_back({5, e0, e1});
+    }
+  }
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
+  return rc;
 }
 
 }  // namespace
@@ -422,9 +630,13 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     return launch(k, 2, dim3((unsigned)((threads + k.nt - 1) / k.nt)), maps, p, stream);
   }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SSM_ERR_CUDA;
+  const ssm::FusedInfo fk = fused_kernel_for(d, conv != nullptr);
+  if (fk.fn)
+    return run_fused(fk, d, sms, dev, x, delta, A, B, C, D, z, delta_bias, out, final_state, stream,
+                     scratch, scratch_bytes);
   if (d.batch > 65535) return SSM_ERR_DIMS;
   Plan pl;
-  if (!make_plan(d, sms, conv != nullptr, &pl)) return SSM_ERR_UNSUPPORTED;
+  if (!make_plan(d, sms, conv != nullptr, &pl, scratch ? scratch_bytes : 0)) return SSM_ERR_UNSUPPORTED;
 
   ScanParams p;
   std::memset(&p, 0, sizeof p);
@@ -471,7 +683,7 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     // the prologue's input history, copied by the aggregate pass: the output pass
     // writes the new history over the same buffer
     const size_t ncs = chist ? (size_t)d.batch * d.dim * 3 : 0;
-    const size_t bytes = (nH + nS + nh0 + ncs) * sizeof(float);
+    const size_t bytes = chunk_ws_bytes(d, pl.nchunks, conv != nullptr);
     if (scratch) {
       if (bytes > scratch_bytes) return SSM_ERR_SCRATCH;
       p.ws_H = static_cast<float*>(scratch);
@@ -713,6 +925,17 @@ int ssm_release_workspace(void) {
 
 uint64_t ssm_kernel_launches(void) { return g_launches.load(); }
 
+int64_t ssm_workspace_reserved_bytes(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (dev >= (int)g_pools.size() || !g_pools[dev]) return 0;
+  cuuint64_t v = 0;
+  if (cudaMemPoolGetAttribute(g_pools[dev], cudaMemPoolAttrReservedMemCurrent, &v) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return (int64_t)v;
+}
+
 int ssm_set_option(const char* name, int64_t value) {
   if (!name || value < 0) return SSM_ERR_DIMS;
   if (!std::strcmp(name, "chunks")) g_opt_chunks = value;
@@ -723,6 +946,8 @@ int ssm_set_option(const char* name, int64_t value) {
   else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
   else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;
   else if (!std::strcmp(name, "inject_stall")) g_opt_inject_stall = std::min<int64_t>(value, INT32_MAX);
+  else if (!std::strcmp(name, "fused")) g_opt_fused = value ? 1 : 0;
+  else if (!std::strcmp(name, "hold_chunk")) g_opt_hold_chunk = std::min<int64_t>(value, INT32_MAX);
   else return SSM_ERR_DIMS;
   return SSM_OK;
 }

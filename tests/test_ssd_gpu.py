@@ -117,15 +117,19 @@ def test_ssd_empty_sequence():
 
 
 def test_ssd_full_size_sampled_heads():
-    """The 2.7B-shaped layer (4 x 4096 steps, 80 heads of 64, N 128) in one call;
-    three sampled (batch row, head) pairs against the oracle run on that head's
-    slice of the inputs."""
+    """The 2.7B-shaped layer (4 x 4096 steps, 80 heads of 64, N 128) in one call, as
+    the benchmark launches it; sixteen (batch row, head) pairs spread over every batch
+    row and the head range (the first and last head included) against the oracle run
+    on that head's slice of the inputs."""
     import torch
     cfg = SSD_CONFIGS["mamba2_2p7b_bf16"]
     w = make_ssd("mamba2_2p7b_bf16", **cfg)
     out, st = ssd_gpu(w)
     G = w.ngroups
-    for b, h in ((0, 0), (1, 37), (3, 79)):
+    rng = np.random.default_rng(2700)
+    pairs = [(0, 0), (3, 79)] + [(int(b), int(h)) for b, h in
+                                 zip(np.arange(14) % w.batch, rng.choice(w.nheads, 14, replace=False))]
+    for b, h in pairs:
         g = h // (w.nheads // G)
         sl = make_ssd("slice", batch=1, seqlen=1, nheads=1, headdim=64, dstate=w.dstate, seed=0)
         sl.batch, sl.seqlen, sl.nheads, sl.ngroups = 1, w.seqlen, 1, 1

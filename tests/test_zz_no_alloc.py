@@ -58,9 +58,34 @@ def test_noalloc_matches_regular_entry_point(name, kw, chunks):
         ssm.ssm_set_option("chunks", 0)
 
 
+def test_noalloc_allocates_nothing():
+    """Forced into chunks, the no-allocation entry point leaves the library's memory pool
+    untouched: with the pool trimmed to nothing first, it still holds nothing after two
+    calls; the regular entry point, given the same call, takes its workspace from it."""
+    import selective_state_space_112_b300 as ssm
+    w = make_workload("pool", batch=1, seqlen=4000, dim=512, dstate=16, io="bf16", seed=5,
+                      state_in=True)
+    dev = device_inputs(w)
+    try:
+        ssm.ssm_set_option("chunks", 8)
+        _run(ssm, w, dev, noalloc=True)          # first call on the device: set-up
+        assert ssm.ssm_release_workspace() == 0
+        before = ssm.ssm_workspace_reserved_bytes()
+        assert before == 0
+        for _ in range(2):
+            _run(ssm, w, dev, noalloc=True)
+            assert ssm.ssm_workspace_reserved_bytes() == before
+        _run(ssm, w, dev, noalloc=False)
+        assert ssm.ssm_workspace_reserved_bytes() > before
+    finally:
+        ssm.ssm_set_option("chunks", 0)
+
+
 def test_noalloc_rejects_a_workspace_beyond_its_scratch():
-    """(chunks - 1) * batch * dim * (N + 1) * 4 bytes above the 16 MiB array: the call
-    returns SSM_ERR_SCRATCH before launching anything."""
+    """A forced chunk count whose workspace ((chunks - 1) * batch * dim * (2 N + 1) * 4
+    bytes and the carry flags) is above the 16 MiB array: the call returns
+    SSM_ERR_SCRATCH before launching anything.  (An automatic chunk count shrinks until
+    its workspace fits instead.)"""
     import torch
     import selective_state_space_112_b300 as ssm
     from selective_state_space_112_b300._abi import SSM_ERR_SCRATCH, SSM_NOALLOC_SCRATCH_BYTES
