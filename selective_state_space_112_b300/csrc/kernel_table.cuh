@@ -1,10 +1,10 @@
 // Kernel lookup for the tiled selective-scan kernel: one entry per (io dtype, B/C
-// layout, input-term form, pass, states per lane S, lanes per channel G).  The
+// layout, input-term form, pass (0: chunk aggregates, 1: output, 2: the whole call in
+// one launch), states per lane S, lanes per channel G).  The
 // instantiations are spread over ten translation units
 // (kernels_<io>_<layout>[_zoh|_conv].cu) so that they build in parallel.
 #pragma once
 
-#include "scan_fused.cuh"
 #include "scan_tile.cuh"
 
 namespace ssm {
@@ -29,7 +29,8 @@ template <typename IO, int S, int G, bool LTI, int PASS, int VAR>
 KernelInfo kernel_info() {
   using Gm = Geo<IO, S, G>;
   KernelInfo k;
-  k.fn = scan_tile_kernel<IO, S, G, LTI, PASS, VAR>;
+  if constexpr (PASS == 2) k.fn = scan_onelaunch_kernel<IO, S, G, LTI, VAR>;
+  else k.fn = scan_tile_kernel<IO, S, G, LTI, PASS, VAR>;
   k.nt = Gm::NT;
   k.ch = Gm::CH;
   k.t = Gm::T;
@@ -48,6 +49,7 @@ KernelInfo pick_sg(int S, int G) {
 
 template <typename IO, bool LTI, int VAR>
 KernelInfo lookup_impl(int S, int G, int pass) {
+  if (pass == 2) return pick_sg<IO, LTI, 2, VAR>(S, G);
   return pass ? pick_sg<IO, LTI, 1, VAR>(S, G) : pick_sg<IO, LTI, 0, VAR>(S, G);
 }
 
@@ -62,22 +64,6 @@ KernelInfo lookup_bf16_tv_zoh(int S, int G, int pass);
 KernelInfo lookup_bf16_lti_zoh(int S, int G, int pass);
 KernelInfo lookup_f32_tv_conv(int S, int G, int pass);
 KernelInfo lookup_bf16_tv_conv(int S, int G, int pass);
-
-// Two-channel kernel with the chunk carry in one launch (scan_fused.cuh), built for
-// time-varying B and C, the fused scan's input term and S = N in {4, 8, 16} (bf16:
-// {8, 16}); kernels_fused.cu.
-typedef void (*FusedFn)(TmaMaps, FusedParams);
-
-struct FusedInfo {
-  FusedFn fn = nullptr;
-  int nt = 0;    // threads per CTA
-  int ch = 0;    // channels per CTA
-  int cw = 0;    // channels per consumer warp
-  int t = 0;     // steps per tile
-  int smem = 0;  // dynamic shared memory bytes
-};
-
-FusedInfo lookup_fused(int io_bf16, int S);
 
 // Recurrent step kernel (sequence length 1), step_kernel.cu: G threads per channel of
 // 4 states each, G in {1, 2, 4, 8, 16}.

@@ -33,7 +33,7 @@ std::atomic<int64_t> g_opt_ctas_per_sm{3};
 std::atomic<int64_t> g_opt_pow_path{1};
 std::atomic<int64_t> g_opt_tma{1};
 std::atomic<int64_t> g_opt_inject_stall{0};  // tests: 1 + tile index the producer withholds
-std::atomic<int64_t> g_opt_fused{1};         // two-channel kernel with the carry in one launch
+std::atomic<int64_t> g_opt_one_launch{0};    // chunked calls in one launch (decoupled lookback)
 std::atomic<int64_t> g_opt_hold_chunk{0};    // tests: 1 + chunk index that never publishes
 std::atomic<uint64_t> g_launches{0};
 
@@ -50,7 +50,7 @@ bool g_prof_on = false;
 std::vector<ProfRec> g_prof;
 constexpr int kKinds = 6;
 const char* const kKindName[kKinds] = {"ssm_chunk_aggregate", "ssm_scan_output", "ssm_step",
-                                      "ssm_bwd_reverse_aggregate", "ssm_bwd_main", "ssm_scan_fused"};
+                                      "ssm_bwd_reverse_aggregate", "ssm_bwd_main", "ssm_scan_one_launch"};
 
 // ------------------------------------------------------- per-device pools
 
@@ -86,7 +86,7 @@ struct Plan {
   bool tma = false;      // TMA-pipelined tiles (else the generic global-memory path)
   int nchunks = 1;
   int64_t chunk_len = 0;
-  ssm::KernelInfo out_k, agg_k;
+  ssm::KernelInfo out_k, agg_k, one_k;
 };
 
 // var 0: the scan as stated; 1: exact ZOH input term; 2: block prologue (conv + silu).
@@ -170,6 +170,38 @@ size_t chunk_ws_bytes(const ssm_dims& d, int64_t k, bool conv) {
   return (nH + nS + nh0 + ncs) * sizeof(float);
 }
 
+// Workspace of the one-launch carry with k chunks: the publication flags and the ticket
+// counter (cleared before every launch), the step sums and end states of chunks
+// 1 .. k-2 (slots indexed by chunk), the first chunk's true end state and a copy of the
+// initial state.
+struct OneLaunchWs {
+  size_t flag_bytes = 0, off_S = 0, off_H = 0, off_P = 0, off_h0 = 0, bytes = 0;
+};
+
+constexpr int kConsumerWarps = 4;  // per CTA of the tiled kernel: one publication flag each
+
+OneLaunchWs one_launch_ws(const ssm_dims& d, int64_t k, int ch) {
+  OneLaunchWs w;
+  if (k <= 1) return w;
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  const int nwb = (int)((d.dim + ch - 1) / ch) * kConsumerWarps;
+  const size_t nflags = (size_t)(k - 1) * d.batch * nwb + 1;
+  const size_t nS = (size_t)(k - 1) * d.batch * d.dim;
+  const size_t st = (size_t)d.batch * d.dim * d.dstate;
+  w.flag_bytes = up(nflags * 4);
+  w.off_S = w.flag_bytes;
+  w.off_H = w.off_S + up(nS * 4);
+  w.off_P = w.off_H + up(nS * d.dstate * 4);
+  w.off_h0 = w.off_P + up(st * 4);
+  w.bytes = w.off_h0 + (d.state_in ? up(st * 4) : 0);
+  return w;
+}
+
+// The workspace a call with k chunks needs, in the carry mode the options select.
+size_t call_ws_bytes(const ssm_dims& d, int64_t k, bool conv, int ch) {
+  return g_opt_one_launch.load() ? one_launch_ws(d, k, ch).bytes : chunk_ws_bytes(d, k, conv);
+}
+
 // Chunks along the sequence only when that leaves fewer than `ctas_per_sm` CTAs per
 // SM: every chunk but the last is then scanned twice (aggregate, output), so the
 // chunk count is the largest that still fits ctas_per_sm CTAs on every SM (one
@@ -208,6 +240,7 @@ bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl, size_t max_ws_by
   const int var = conv ? 2 : d.bbar_mode;
   pl->out_k = lookup(d.io_dtype, lti, pl->S, G, 1, var);
   pl->agg_k = lookup(d.io_dtype, lti, pl->S, G, 0, var);
+  pl->one_k = lookup(d.io_dtype, lti, pl->S, G, 2, var);
   pl->tma = g_opt_tma.load() && tma_ok(d);
   int64_t k = g_opt_chunks.load();
   if (k <= 0) {
@@ -231,7 +264,8 @@ bool make_plan(const ssm_dims& d, int sms, bool conv, Plan* pl, size_t max_ws_by
   split(k);
   if (max_ws_bytes && g_opt_chunks.load() <= 0) {
     // a fixed scratch: fewer automatic chunks until the workspace fits
-    while (pl->nchunks > 1 && chunk_ws_bytes(d, pl->nchunks, conv) > max_ws_bytes) split(pl->nchunks - 1);
+    while (pl->nchunks > 1 && call_ws_bytes(d, pl->nchunks, conv, pl->out_k.ch) > max_ws_bytes)
+      split(pl->nchunks - 1);
   }
   return true;
 }
@@ -316,198 +350,10 @@ int launch_bwd(ssm::BwdFn fn, int kind, dim3 grid, const ssm::BwdParams& p, cuda
   return SSM_OK;
 }
 
-// ------------------------------------------------- two-channel fused kernel
-
-// The fused kernel serves time-varying B and C, the fused scan's input term, no
-// prologue, shapes a tensor map can describe, and N in {4, 8, 16} (bf16: 8, 16).
-ssm::FusedInfo fused_kernel_for(const ssm_dims& d, bool conv) {
-  if (!g_opt_fused.load() || conv || d.bbar_mode != 0 || d.bc_layout != SSM_BC_TIME_VARYING ||
-      !g_opt_tma.load() || !tma_ok(d) || (g_opt_lanes.load() > 1))
-    return ssm::FusedInfo();
-  if (d.dstate != 4 && d.dstate != 8 && d.dstate != 16) return ssm::FusedInfo();
-  return ssm::lookup_fused(d.io_dtype == SSM_BF16, (int)d.dstate);
-}
-
-bool prepare_fused(const ssm::FusedInfo& k) {
-  static std::mutex mu;
-  static std::vector<const void*> done;
-  std::lock_guard<std::mutex> lk(mu);
-  for (auto f : done)
-    if (f == (const void*)k.fn) return true;
-  if (cudaFuncSetAttribute((const void*)k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
-      cudaSuccess)
-    return false;
-  done.push_back((const void*)k.fn);
-  return true;
-}
-
-int fused_occupancy(const ssm::FusedInfo& k) {
-  static std::mutex mu;
-  static std::vector<std::pair<const void*, int>> cache;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    for (auto& e : cache)
-      if (e.first == (const void*)k.fn) return e.second;
-  }
-  int occ = 0;
-  if (!prepare_fused(k) ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)k.fn, k.nt, k.smem) != cudaSuccess ||
-      occ < 1)
-    occ = 1;
-  std::lock_guard<std::mutex> lk(mu);
-  cache.push_back({(const void*)k.fn, occ});
-  return occ;
-}
-
-// Longest chunk: a chunk's first scan is the longest time a CTA waits for another
-// (every wait of the kernels gives up after 2 s), so chunks stay short enough.
-constexpr int64_t kMaxChunkLen = 1 << 18;
-
-// Workspace of the fused kernel with k chunks: flags and the ticket counter (zeroed
-// before every launch), then the step sums, aggregates and prefixes of chunks
-// 0 .. k-2, then a copy of the initial state.
-struct FusedWs {
-  size_t flag_bytes = 0, bytes = 0;
-  size_t off_S = 0, off_H = 0, off_P = 0, off_h0 = 0;
-};
-
-FusedWs fused_ws(const ssm_dims& d, int64_t k, int nwb) {
-  FusedWs w;
-  if (k <= 1) return w;
-  const size_t nflags = (size_t)(k - 1) * d.batch * nwb + 1;
-  w.flag_bytes = (nflags * 4 + 255) / 256 * 256;
-  const size_t nS = (size_t)(k - 1) * d.batch * d.dim;
-  const size_t nH = nS * d.dstate;
-  w.off_S = w.flag_bytes;
-  w.off_H = w.off_S + (nS * 4 + 255) / 256 * 256;
-  w.off_P = w.off_H + nH * 4;
-  w.off_h0 = w.off_P + nH * 4;
-  w.bytes = w.off_h0 + (d.state_in ? (size_t)d.batch * d.dim * d.dstate * 4 : 0);
-  return w;
-}
-
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + nb && y < x + na;
-}
-
-// One call on the fused kernel (see scan_fused.cuh): plan the chunks, take the
-// workspace, clear its flags, encode the tensor maps, launch once.
-int run_fused(const ssm::FusedInfo& fk, const ssm_dims& d, int sms, int dev, const void* x,
-              const void* delta, const float* A, const void* B, const void* C, const float* D,
-              const void* z, const float* delta_bias, void* out, float* final_state,
-              cudaStream_t stream, void* scratch, size_t scratch_bytes) {
-  if (!prepare_fused(fk)) return SSM_ERR_CUDA;
-  const int ncb = (int)((d.dim + fk.ch - 1) / fk.ch);
-  const int nwb = ncb * (fk.ch / fk.cw);
-  const int64_t per_chunk = d.batch * ncb;
-  const int64_t max_chunks = (d.seqlen + ssm::kChunkAlign - 1) / ssm::kChunkAlign;
-  int64_t k = g_opt_chunks.load();
-  const bool forced = k > 0;
-  if (!forced) {
-    // as many chunks as fill every SM with the kernel's resident CTAs in one wave
-    const int64_t slots = (int64_t)sms * fused_occupancy(fk);
-    k = per_chunk >= slots ? 1 : slots / per_chunk;
-    const int64_t min_len = std::max<int64_t>(ssm::kChunkAlign, g_opt_min_chunk_len.load());
-    k = std::min<int64_t>(k, std::max<int64_t>(1, d.seqlen / min_len));
-  }
-  k = std::max<int64_t>(k, (d.seqlen + kMaxChunkLen - 1) / kMaxChunkLen);
-  k = std::max<int64_t>(1, std::min<int64_t>(k, max_chunks));
-  auto split = [&](int64_t kk, int64_t* len, int* nch) {
-    int64_t l = (d.seqlen + kk - 1) / kk;
-    l = (l + ssm::kChunkAlign - 1) / ssm::kChunkAlign * ssm::kChunkAlign;
-    *len = l;
-    *nch = (int)((d.seqlen + l - 1) / l);
-  };
-  int64_t len = 0;
-  int nch = 1;
-  split(k, &len, &nch);
-  if (scratch) {
-    // the fixed scratch: fewer chunks until the workspace fits (a forced count does not shrink)
-    while (nch > 1 && fused_ws(d, nch, nwb).bytes > scratch_bytes) {
-      if (forced || len >= kMaxChunkLen) return SSM_ERR_SCRATCH;
-      split(nch - 1, &len, &nch);
-    }
-  }
-  if ((int64_t)nch * per_chunk > INT32_MAX) return SSM_ERR_DIMS;
-
-  ssm::FusedParams p;
-  std::memset(&p, 0, sizeof p);
-  p.x = x; p.delta = delta; p.z = z; p.out = out; p.A = A; p.B = B; p.C = C;
-  p.Dskip = D; p.bias = delta_bias; p.final_state = final_state;
-  p.h_init = d.state_in ? final_state : nullptr;
-  p.batch = d.batch; p.seqlen = d.seqlen; p.dim = d.dim; p.dstate = (int)d.dstate;
-  p.nchunks = nch; p.chunk_len = len; p.ncb = ncb; p.nwb = nwb;
-  p.delta_softplus = d.delta_softplus;
-  p.pow_path = (int)g_opt_pow_path.load();
-  p.stall_tile = (int)g_opt_inject_stall.load() - 1;
-  p.hold_chunk = (int)g_opt_hold_chunk.load() - 1;
-  int* status = nullptr;
-  if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return SSM_ERR_CUDA;
-  p.status = status;
-
-  const size_t esz = d.io_dtype == SSM_BF16 ? 2 : 4;
-  const int eb = (int)esz;
-  ssm::TmaMaps maps;
-  std::memset(&maps, 0, sizeof maps);
-  bool okm = encode3d(&maps.x, x, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
-             encode3d(&maps.delta, delta, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
-             encode3d(&maps.out, out, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t) &&
-             encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, fk.t) &&
-             encode3d(&maps.C, C, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, fk.t);
-  if (okm && z) okm = encode3d(&maps.z, z, eb, d.dim, d.seqlen, d.batch, fk.ch, fk.t);
-  if (!okm) return SSM_ERR_CUDA;
-
-  void* ws = nullptr;
-  if (nch > 1) {
-    const FusedWs w = fused_ws(d, nch, nwb);
-    unsigned char* base = nullptr;
-    if (scratch) {
-      base = static_cast<unsigned char*>(scratch);
-    } else {
-      cudaMemPool_t pool;
-      if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
-      if (cudaMallocFromPoolAsync(&ws, w.bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
-      base = static_cast<unsigned char*>(ws);
-    }
-    p.flags = reinterpret_cast<unsigned*>(base);
-    p.ticket = p.flags + (size_t)(nch - 1) * d.batch * nwb;
-    p.agg_S = reinterpret_cast<float*>(base + w.off_S);
-    p.agg_H = reinterpret_cast<float*>(base + w.off_H);
-    p.pre_H = reinterpret_cast<float*>(base + w.off_P);
-    p.ws_h0 = d.state_in ? reinterpret_cast<float*>(base + w.off_h0) : nullptr;
-    if (cudaMemsetAsync(base, 0, w.flag_bytes, stream) != cudaSuccess) {
-      if (ws) cudaFreeAsync(ws, stream);
-      return SSM_ERR_CUDA;
-    }
-  }
-
-  cudaEvent_t e0 = nullptr, e1 = nullptr;
-  bool prof;
-  {
-    std::lock_guard<std::mutex> lk(g_prof_mu);
-    prof = g_prof_on;
-  }
-  int rc = SSM_OK;
-  if (prof && (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
-               cudaEventRecord(e0, stream) != cudaSuccess))
-    rc = SSM_ERR_CUDA;
-  if (rc == SSM_OK) {
-    fk.fn<<<dim3((unsigned)(nch * per_chunk)), fk.nt, fk.smem, stream>>>(maps, p);
-    if (cudaGetLastError() != cudaSuccess) rc = SSM_ERR_CUDA;
-    else g_launches.fetch_add(1);
-  }
-  if (rc == SSM_OK && prof) {
-    if (cudaEventRecord(e1, stream) != cudaSuccess) {
-      rc = SSM_ERR_CUDA;
-    } else {
-      std::lock_guard<std::mutex> lk(g_prof_mu);
-      g_prof.push_back({5, e0, e1});
-    }
-  }
-  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
-  return rc;
 }
 
 }  // namespace
@@ -630,10 +476,6 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
     return launch(k, 2, dim3((unsigned)((threads + k.nt - 1) / k.nt)), maps, p, stream);
   }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SSM_ERR_CUDA;
-  const ssm::FusedInfo fk = fused_kernel_for(d, conv != nullptr);
-  if (fk.fn)
-    return run_fused(fk, d, sms, dev, x, delta, A, B, C, D, z, delta_bias, out, final_state, stream,
-                     scratch, scratch_bytes);
   if (d.batch > 65535) return SSM_ERR_DIMS;
   Plan pl;
   if (!make_plan(d, sms, conv != nullptr, &pl, scratch ? scratch_bytes : 0)) return SSM_ERR_UNSUPPORTED;
@@ -673,6 +515,37 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
       okm = encode3d(&maps.B, B, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T) &&
             encode3d(&maps.C, C, eb, d.dstate, d.seqlen, d.batch, (int)d.dstate, T);
     if (!okm) return SSM_ERR_CUDA;
+  }
+
+  if (pl.nchunks > 1 && g_opt_one_launch.load()) {
+    // the whole call in one launch: aggregates published with flags, decoupled lookback
+    const OneLaunchWs w = one_launch_ws(d, pl.nchunks, ch);
+    const int64_t nblocks = (int64_t)pl.nchunks * d.batch * gx;
+    if (nblocks > INT32_MAX) return SSM_ERR_DIMS;
+    void* ws1 = nullptr;
+    unsigned char* base = nullptr;
+    if (scratch) {
+      if (w.bytes > scratch_bytes) return SSM_ERR_SCRATCH;
+      base = static_cast<unsigned char*>(scratch);
+    } else {
+      cudaMemPool_t pool;
+      if (get_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+      if (cudaMallocFromPoolAsync(&ws1, w.bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+      base = static_cast<unsigned char*>(ws1);
+    }
+    p.ncb = (int)gx;
+    p.nwb = (int)gx * kConsumerWarps;
+    p.hold_chunk = (int)g_opt_hold_chunk.load() - 1;
+    p.flags = reinterpret_cast<unsigned*>(base);
+    p.ticket = p.flags + (size_t)(pl.nchunks - 1) * d.batch * p.nwb;
+    p.ws_S = reinterpret_cast<float*>(base + w.off_S);
+    p.ws_H = reinterpret_cast<float*>(base + w.off_H);
+    p.ws_P = reinterpret_cast<float*>(base + w.off_P);
+    p.ws_h0 = d.state_in ? reinterpret_cast<float*>(base + w.off_h0) : nullptr;
+    int rc = cudaMemsetAsync(base, 0, w.flag_bytes, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    if (rc == SSM_OK) rc = launch(pl.one_k, 5, dim3((unsigned)nblocks), maps, p, stream);
+    if (ws1 && cudaFreeAsync(ws1, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
+    return rc;
   }
 
   void* ws = nullptr;
@@ -946,7 +819,7 @@ int ssm_set_option(const char* name, int64_t value) {
   else if (!std::strcmp(name, "pow_path")) g_opt_pow_path = value ? 1 : 0;
   else if (!std::strcmp(name, "tma")) g_opt_tma = value ? 1 : 0;
   else if (!std::strcmp(name, "inject_stall")) g_opt_inject_stall = std::min<int64_t>(value, INT32_MAX);
-  else if (!std::strcmp(name, "fused")) g_opt_fused = value ? 1 : 0;
+  else if (!std::strcmp(name, "one_launch")) g_opt_one_launch = value ? 1 : 0;
   else if (!std::strcmp(name, "hold_chunk")) g_opt_hold_chunk = std::min<int64_t>(value, INT32_MAX);
   else return SSM_ERR_DIMS;
   return SSM_OK;

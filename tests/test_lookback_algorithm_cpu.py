@@ -1,17 +1,18 @@
-"""The chunk carry of the fused forward kernel, emulated on the CPU in float64.
+"""The one-launch chunk carry of the forward kernel, emulated on the CPU in float64.
 
 The kernel cuts the sequence into chunks; each chunk's first scan starts from a zero
-state (the first chunk from the initial state) and publishes its step sum S_c and end
-state H_c; a chunk's carry-in is then found by walking back over the preceding chunks,
-  H_acc += exp(A S_acc) H_j,  S_acc += S_j   (j = c-1, c-2, ... until an inclusive
-  prefix P_j, the true state at the end of chunk j, which is added as exp(A S_acc) P_j),
-and it publishes its own inclusive prefix exp(A S_c) h_in + H_c.  This is the
-associative combine of the per-step maps ("State-space models", The parallel scan;
-"Structured State Space Models and Mamba", Hardware-Aware Parallel Associative Scan)
-applied to chunk aggregates.  Here the aggregates come from the oracle run on each
-chunk alone, the walk is done in the kernel's order with every mix of published
-aggregates and prefixes, and the carry-ins must equal the oracle's own state at the
-chunk boundaries.
+state (the first chunk from the initial state, so that its end state is the true one)
+and publishes its step sum S_c and end state H_c; a chunk's carry-in is then folded
+from all earlier chunks in a fixed order, from the previous chunk back to the first,
+  H_acc += exp(A S_acc) H_j,  S_acc += S_j   (j = c-1, c-2, ..., 1; then chunk 0's
+  true end state is added as exp(A S_acc) H_0).
+This is the associative combine of the per-step maps ("State-space models", The
+parallel scan; "Structured State Space Models and Mamba", Hardware-Aware Parallel
+Associative Scan) applied to chunk aggregates.  The walk may also stop early at any
+chunk whose true end state (inclusive prefix) is known: the emulation checks every
+such mix, and that the prefix a chunk would publish, exp(A S_c) h_in + H_c, is its
+true end state.  The aggregates come from the oracle run on each chunk alone; the
+carry-ins must equal the oracle's own states at the chunk boundaries.
 """
 import itertools
 

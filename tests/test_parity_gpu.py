@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _options():
     import selective_state_space_112_b300 as ssm
-    defaults = dict(chunks=0, pow_path=1, tma=1, lanes=0, fused=1, hold_chunk=0)
+    defaults = dict(chunks=0, pow_path=1, tma=1, lanes=0, hold_chunk=0, one_launch=0)
     for k, v in defaults.items():
         ssm.ssm_set_option(k, v)
     yield
@@ -337,14 +337,15 @@ def test_copy_wait_timeout_is_reported_and_the_context_stays_usable():
 
 
 def test_lookback_wait_timeout_is_reported_and_the_context_stays_usable():
-    """The chunk carry of the fused kernel without a GPU fault: chunk 2 is told never to
-    publish its aggregate or prefix, so the lookback waits of the chunks after it run out
-    (after 2 s).  The kernel returns, ssm_check_status reports SSM_ERR_TIMEOUT, and the
-    next call matches the oracle."""
+    """The one-launch chunk carry without a GPU fault: chunk 2 is told never to publish
+    its aggregate, so the lookback waits of the chunks after it run out (after 2 s).
+    The kernel returns, ssm_check_status reports SSM_ERR_TIMEOUT, and the next call
+    matches the oracle."""
     import torch
     import selective_state_space_112_b300 as ssm
     w = make_workload("hold", batch=1, seqlen=2000, dim=256, dstate=16, io="bf16", seed=18)
     dev = device_inputs(w)
+    ssm.ssm_set_option("one_launch", 1)
     try:
         ssm.ssm_set_option("hold_chunk", 3)
         ssm.ssm_set_option("chunks", 6)
@@ -359,9 +360,10 @@ def test_lookback_wait_timeout_is_reported_and_the_context_stays_usable():
     full_check(w, "after lookback timeout")
 
 
-FUSED_CASES = [
-    # (name, make_workload kwargs, forced chunk count): shapes the two-channel kernel
-    # takes, run on it and on the two-kernel path
+CARRY_CASES = [
+    # (name, make_workload kwargs, forced chunk count): chunked calls, carried across
+    # chunks by the two launches (aggregate pass, output pass) or by one launch
+    # (aggregates published with flags, decoupled lookback)
     ("chunks9_state_in", dict(batch=2, seqlen=1000, dim=512, dstate=16, state_in=True), 9),
     ("one_chunk", dict(batch=3, seqlen=333, dim=264, dstate=16), 1),
     ("ragged_tail", dict(batch=1, seqlen=1001, dim=136, dstate=16), 5),
@@ -369,23 +371,36 @@ FUSED_CASES = [
     ("s4d_pow", dict(batch=2, seqlen=640, dim=128, dstate=16, a_init="s4d_real", state_in=True), 3),
     ("no_gate_no_D_no_bias", dict(batch=1, seqlen=500, dim=256, dstate=16, gate=False,
                                   with_D=False, with_bias=False), 4),
+    ("lti", dict(batch=2, seqlen=600, dim=64, dstate=16, lti=True, with_bias=False), 5),
     ("auto_plan", dict(batch=1, seqlen=8192, dim=512, dstate=16), 0),
+    ("more_chunks_than_a_wave", dict(batch=2, seqlen=12000, dim=1024, dstate=16), 300),
 ]
 
 
-@pytest.mark.parametrize("fused", [1, 0])
+@pytest.mark.parametrize("one_launch", [0, 1])
+@pytest.mark.parametrize("lanes", [1, 2, 4])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("name,kw,chunks", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
-def test_fused_and_two_kernel_paths(name, kw, chunks, io, fused):
-    """The chunk carry in one launch (decoupled lookback over chunk aggregates) and the
-    two-launch carry (aggregate pass, then output pass), both against the oracle."""
+@pytest.mark.parametrize("name,kw,chunks", CARRY_CASES, ids=[c[0] for c in CARRY_CASES])
+def test_chunk_carry(name, kw, chunks, io, lanes, one_launch):
+    """Both chunk carries on every lane split against the oracle: two launches, and one
+    launch in which each chunk scans itself from a zero state, publishes its aggregate
+    and folds all earlier chunks' aggregates (with more chunks than one wave of CTAs the
+    later CTAs find their predecessors already published)."""
     import selective_state_space_112_b300 as ssm
-    if io == "bf16" and kw["dstate"] < 8:
-        pytest.skip("no tensor map for bf16 rows of fewer than 8 states")
-    ssm.ssm_set_option("fused", fused)
+    ssm.ssm_set_option("one_launch", one_launch)
+    ssm.ssm_set_option("lanes", lanes)
     ssm.ssm_set_option("chunks", chunks)
-    try:
-        w = make_workload(name, io=io, seed=zlib.crc32(("fz" + name + io).encode()) % 1000, **kw)
-        full_check(w, f"{name}/{io}/fused{fused}")
-    finally:
-        ssm.ssm_set_option("fused", 1)
+    w = make_workload(name, io=io, seed=zlib.crc32(("cc" + name + io).encode()) % 1000, **kw)
+    full_check(w, f"{name}/{io}/G{lanes}/one_launch{one_launch}")
+
+
+def test_one_launch_deterministic_bitwise():
+    """The one-launch carry folds the aggregates in a fixed order: two calls agree bit
+    for bit whatever order the chunks finished in."""
+    import selective_state_space_112_b300 as ssm
+    ssm.ssm_set_option("one_launch", 1)
+    w = make_workload("det1", batch=1, seqlen=6000, dim=512, dstate=16, io="bf16", seed=19)
+    dev = device_inputs(w)
+    a = run_gpu(w, dev)
+    b = run_gpu(w, dev)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
