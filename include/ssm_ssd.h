@@ -20,9 +20,10 @@
  *
  * It is the S6 scan of ssm_scan.h with the decay, the step and D tied per head
  * and B, C shared by the heads of a group.  The kernel evaluates it chunk by
- * chunk (64 steps) in the dual form: within a chunk the masked product
- * (L o C B^T)(step x) on the tensor cores; across chunks the (P, N) state of the
- * head, carried on chip; the expanded state never reaches device memory.
+ * chunk (128 steps) in the dual form: within a chunk the masked product
+ * (L o C B^T)(step x) on the 5th-generation tensor cores (tcgen05, accumulators in
+ * tensor memory, inputs staged by TMA); across chunks the (P, N) state of the
+ * head, carried in tensor memory; the expanded state never reaches device memory.
  *
  * Conventions as in ssm_scan.h: device pointers on the current device,
  * contiguous row-major, 16-byte aligned, owned by the caller; the call enqueues
@@ -73,7 +74,10 @@ typedef struct {
  * SSM_ERR_DIMS (a size out of range, ngroups not dividing nheads, an unknown flag
  * value, state_in without final_state), SSM_ERR_ALIGN, SSM_ERR_OVERLAP,
  * SSM_ERR_UNSUPPORTED (io dtype, headdim or dstate this build does not cover),
- * SSM_ERR_CUDA (launch failure or no usable device).
+ * SSM_ERR_CUDA (launch failure or no usable device).  A wait inside the kernel
+ * that does not end within 2 s leaves the call's outputs undefined; the kernel
+ * then frees what it holds and returns, and ssm_check_status reports
+ * SSM_ERR_TIMEOUT.
  * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation.  The
  * operands formed inside the kernel (the masked decay matrix, the decay-weighted
  * inputs and the carried state, all fp32) enter as a pair of bf16 values (value

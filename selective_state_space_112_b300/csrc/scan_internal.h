@@ -28,4 +28,12 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
 // Counts one kernel launch of the library (read by ssm_kernel_launches).
 void count_launch();
 
+// Device address of the status word the kernels raise (read by ssm_check_status), or
+// null if the runtime cannot give it.
+int* status_word();
+
+// Options of the SSD layer (ssm_set_option forwards names it does not know): returns
+// true if the name is one of them.
+bool set_ssd_option(const char* name, int64_t value);
+
 }  // namespace ssm_internal

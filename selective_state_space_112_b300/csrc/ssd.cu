@@ -19,14 +19,19 @@
 // lo = bf16(v - hi), with one product each: about 16 significant bits, where one
 // bf16 rounding (8 bits) of the state would show in y at the 1e-2 level.  C, B and x
 // are bf16 inputs and exact.  Inputs stream through a two-stage cp.async ring.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
 #include <atomic>
+#include <cstring>
+#include <mutex>
 
 #include "scan_internal.h"
+#include "ssd_tc.cuh"
 #include "ssm_ssd.h"
 
 namespace {
@@ -500,6 +505,71 @@ int launch_ssd(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// ------------------------------------------------ the tcgen05 kernel (ssd_tc.cuh)
+
+std::atomic<int64_t> g_ssd_legacy{0};  // 1: the mma.sync kernel above instead
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A (inner, mid, L, batch) bf16 tensor, boxes of 8 inner values x 1 x Q steps x 1: one
+// block of 8 columns of a chunk, laid out as Q rows of 16 bytes.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2),
+                                 (cuuint64_t)(inner * mid * L * 2)};
+  const cuuint32_t box[4] = {8, 1, (cuuint32_t)ssd::Q, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NP, int PB>
+int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t stream) {
+  using Sm = ssd::Smem<NP, PB>;
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(ready.load() & bit)) {
+    if (cudaFuncSetAttribute(ssd::ssd_tc_kernel<NP, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Sm::BYTES) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    ready.fetch_or(bit);
+  }
+  ssd::Maps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (!encode_rows(&maps.x, prm.x, P, prm.H, prm.L, batch) ||
+      !encode_rows(&maps.B, prm.B, N, prm.G, prm.L, batch) ||
+      !encode_rows(&maps.C, prm.C, N, prm.G, prm.L, batch))
+    return SSM_ERR_CUDA;
+  ssd::Params p;
+  std::memset(&p, 0, sizeof p);
+  p.x = prm.x; p.dt = prm.dt; p.z = prm.z; p.A = prm.A; p.D = prm.D; p.dt_bias = prm.dt_bias;
+  p.out = prm.out; p.state = prm.state; p.L = prm.L; p.H = prm.H; p.G = prm.G; p.hpg = prm.hpg;
+  p.N = N; p.softplus = prm.softplus; p.state_in = prm.state_in;
+  p.status = ssm_internal::status_word();
+  if (!p.status) return SSM_ERR_CUDA;
+  ssd::ssd_tc_kernel<NP, PB><<<dim3((unsigned)prm.H * (ssd::P / PB), (unsigned)batch), ssd::NTHR, Sm::BYTES,
+                               stream>>>(maps, p);
+  ssm_internal::count_launch();
+  return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
@@ -564,9 +634,28 @@ extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const 
   prm.hpg = (int)(d.nheads / d.ngroups);
   prm.softplus = d.dt_softplus;
   prm.state_in = d.state_in;
+  if (!g_ssd_legacy.load()) {
+    switch (d.dstate) {
+      case 64: return launch_ssd_tc<128, 32>(prm, d.batch, 64, stream);  // state rows padded to 128
+      case 128: return launch_ssd_tc<128, 32>(prm, d.batch, 128, stream);
+      default: return launch_ssd_tc<256, 32>(prm, d.batch, 256, stream);
+    }
+  }
   switch (d.dstate) {
     case 64: return launch_ssd<64, 64>(prm, d.batch, stream);
     case 128: return launch_ssd<128, 64>(prm, d.batch, stream);
     default: return launch_ssd<256, 32>(prm, d.batch, stream);  // half a head per CTA
   }
 }
+
+namespace ssm_internal {
+
+bool set_ssd_option(const char* name, int64_t value) {
+  if (!std::strcmp(name, "ssd_legacy")) {
+    g_ssd_legacy = value ? 1 : 0;
+    return true;
+  }
+  return false;
+}
+
+}  // namespace ssm_internal

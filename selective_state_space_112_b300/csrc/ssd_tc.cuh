@@ -1,0 +1,587 @@
+// Mamba-2 SSD layer, forward, on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// Pages: "State-space models", section "The parallel scan" (A a scalar times the
+// identity per head turns the scan into blocks of matrix products on the tensor
+// cores); "Structured State Space Models and Mamba", section "State Space Duality and
+// Mamba-2" (Y = (L o (C B^T)) V with a 1-semiseparable decay mask L).
+//
+// One CTA (four warps, 128 threads) owns one (batch row, head, block of PB channels)
+// and walks the sequence in chunks of Q = 128 steps, the (N, PB) state of its channels
+// carried in tensor memory.  With S_i the running sum of step * A inside a chunk:
+//   G        = C B^T                                          (Q x Q over N)
+//   M[i][j]  = G[i][j] exp(S_i - S_j) step_j   for j <= i, else 0
+//   Yd       = M X                                            (Q x PB over Q)
+//   Yo       = C h_prev                                       (Q x PB over N)
+//   y_i      = Yd_i + exp(S_i) Yo_i + D x_i;   out = y silu(z)
+//   h_next   = exp(S_last) h_prev + B^T Xw,   Xw_j = exp(S_last - S_j) step_j x_j
+// The four products are tcgen05.mma (kind::f16: bf16 operands, fp32 accumulators in
+// TMEM), issued by one thread and completed on mbarriers.  Operands sit in shared
+// memory in the no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix,
+// blocks of 8 columns stored one after another): C, B and x arrive that way by TMA
+// tensor copies (one box of 8 columns x Q rows per block); M, Xw and the state copy
+// are written there by the threads.  Thread i owns TMEM lane i (row i of every
+// accumulator) for the element-wise work.
+//
+// Order inside a chunk: G is issued as soon as the inputs land; while it runs the
+// threads form Xw and the state copy, then C h_prev and B^T Xw are issued; M is formed
+// from G once those products are done, into the space of C and B (no longer read),
+// and M X is issued last.  The decay factor of M is split as
+//   exp(S_i - S_j) = exp(S_i - S_ref) exp(S_ref - S_j),  S_ref = the midpoint of the
+// chunk's range of S, so that M costs two multiplies per element; a chunk whose range
+// of S is too wide for both factors to stay inside fp32 takes one exponential per
+// element instead.  Rows above the diagonal block of a warp are zero and not formed.
+//
+// Precision: the operands formed in fp32 enter as a pair of bf16 values (value and
+// remainder, about 16 significant bits): M (one bf16 rounding of it would cost up to
+// about 1e-2 of floored error on Gaussian inputs), Xw and the state copy (the state
+// accumulates over the whole sequence).  Step sizes, decays and the state stay in
+// fp32.  Every wait is bounded (2 s); a wait that runs out sets the status word and
+// the CTA waits (bounded) for its products in flight, frees its tensor memory and
+// leaves.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ssd {
+
+constexpr int Q = 128;      // steps per chunk (the M dimension of every product)
+constexpr int P = 64;       // channels per head
+constexpr int NTHR = 128;   // threads per CTA: one per TMEM lane
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct Maps {
+  CUtensorMap x;   // (P, H, L, batch), box (8, 1, Q, 1)
+  CUtensorMap B;   // (N, G, L, batch), box (8, 1, Q, 1)
+  CUtensorMap C;
+};
+
+struct Params {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* dt;
+  const __nv_bfloat16* z;
+  const float* A;
+  const float* D;
+  const float* dt_bias;
+  __nv_bfloat16* out;
+  float* state;       // (batch, H, P, N) or null
+  int* status;
+  int64_t L;
+  int H, G, hpg, N;
+  int softplus, state_in;
+};
+
+// Shared-memory plan of one CTA: NP = N padded to a multiple of 128 (the state rows
+// of one product), PB channels.  M (hi, lo) reuses the space of C and B.
+template <int NP, int PB>
+struct Smem {
+  static constexpr int C_OFF = 0;                        // C tile  [Q x NP] bf16
+  static constexpr int B_OFF = C_OFF + Q * NP * 2;       // B tile  [Q x NP]
+  static constexpr int M_OFF = 0;                        // M hi, lo [Q x Q] each
+  static constexpr int X_OFF = B_OFF + Q * NP * 2;       // x tile  [Q x PB]
+  static constexpr int W_OFF = X_OFF + Q * PB * 2;       // Xw hi, lo [Q x PB] each
+  static constexpr int H_OFF = W_OFF + 2 * Q * PB * 2;   // state hi, lo [NP x PB] each
+  static constexpr int V_OFF = H_OFF + 2 * NP * PB * 2;  // S, step, b (Q floats each), reductions
+  static constexpr int BAR_OFF = V_OFF + 3 * Q * 4 + 64;
+  static constexpr int BYTES = BAR_OFF + 64;
+  // TMEM columns: G, Yd, Yo, state (NP / 128 blocks of PB)
+  static constexpr int T_G = 0, T_YD = Q, T_YO = Q + PB, T_H = Q + 2 * PB;
+  static constexpr int TUSED = T_H + (NP / 128) * PB;
+  static constexpr int TCOLS = TUSED <= 256 ? 256 : 512;
+  static_assert(TUSED <= 512, "tensor memory columns");
+  static_assert(2 * Q * Q * 2 <= X_OFF, "M (hi, lo) fits in the space of C and B");
+  static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t par) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(par)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: false if it did not complete within kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t par) {
+  if (mbar_try(bar, par)) return true;
+  const uint64_t t0 = gtimer();
+  for (long long i = 0; i < (1ll << 30); ++i) {
+    if (mbar_try(bar, par)) return true;
+    if (gtimer() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
+
+// Shared-memory matrix descriptor, no swizzle: start address, leading-dimension byte
+// offset (between core matrices along K), stride-dimension byte offset (between core
+// matrices along M or N), the fixed version bits.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N, K-major (0) or
+// MN-major (1) A and B.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// v = hi + lo with both parts bf16 (lo holds what hi rounds away)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Byte offset of row r, column block cb (8 columns) in a no-swizzle core-matrix tile of
+// R rows whose column blocks are stored one after another (block cb at cb * R * 16).
+__device__ __forceinline__ uint32_t cm(int r, int cb, int R) { return (uint32_t)(cb * R + r) * 16u; }
+
+template <int NP, int PB>
+__global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 1)
+    ssd_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  using Sm = Smem<NP, PB>;
+  constexpr float kLog2e = 1.4426950408889634f;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x / (P / PB), pc = (blockIdx.x % (P / PB)) * PB;  // head, first channel
+  const int b = blockIdx.y, g = h / p.hpg;
+  const int64_t L = p.L;
+  const int nch = (int)((L + Q - 1) / Q);
+  const int N = p.N, kN = p.N / 16;  // K steps over the state dimension
+  const float Ah = p.A[h], Dh = p.D ? p.D[h] : 0.f, biash = p.dt_bias ? p.dt_bias[h] : 0.f;
+  float* Sv = reinterpret_cast<float*>(smem + Sm::V_OFF);  // S_i of the chunk
+  float* stepv = Sv + Q;                                  // step_i
+  float* bv = stepv + Q;                                  // exp(S_ref - S_j) step_j
+  float* red = bv + Q;                                    // per-warp sums, minima, maxima
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::BAR_OFF);
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(bars + 4);
+  const uint32_t bar_in = su32(&bars[0]), bar_g = su32(&bars[1]), bar_s = su32(&bars[2]),
+                 bar_y = su32(&bars[3]);
+  const uint32_t s_base = su32(smem);
+
+  // zero the tiles once (the rows of B past N feed state rows that are never read)
+  for (int i = tid; i < Sm::V_OFF / 16; i += NTHR) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[i])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tbase_s)),
+                 "r"(Sm::TCOLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase_s;
+  const uint32_t lane_t = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  bool ok = true;
+  int issued = 0;  // products issued and not yet waited for: bit 0 G, 1 C h / B^T Xw, 2 M X
+
+  // the state: h_{-1} (or zeros) into TMEM, lane n = state n, columns of PB channels
+  {
+    const int64_t sb = ((int64_t)b * p.H + h) * P * N;
+#pragma unroll 1
+    for (int nb = 0; nb < NP / 128; ++nb) {
+      const int n = nb * 128 + tid;
+#pragma unroll 1
+      for (int c0 = 0; c0 < PB; c0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = (p.state_in && n < N) ? p.state[sb + (int64_t)(pc + c0 + j) * N + n] : 0.f;
+        tmem_st32(lane_t + Sm::T_H + nb * PB + c0, v);
+      }
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  }
+
+  // the inputs of chunk c: C, B (N / 8 column blocks) and x (PB / 8 blocks) by TMA
+  const uint32_t in_bytes = (uint32_t)((2 * (N / 8) + PB / 8) * Q * 16);
+  auto load_chunk = [&](int c) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_in), "r"(in_bytes)
+                 : "memory");
+    const int t0 = c * Q;
+    for (int kb = 0; kb < N / 8; ++kb) {
+      tma_load_4d(s_base + Sm::C_OFF + kb * Q * 16, &maps.C, kb * 8, g, t0, b, bar_in);
+      tma_load_4d(s_base + Sm::B_OFF + kb * Q * 16, &maps.B, kb * 8, g, t0, b, bar_in);
+    }
+    for (int kb = 0; kb < PB / 8; ++kb)
+      tma_load_4d(s_base + Sm::X_OFF + kb * Q * 16, &maps.x, pc + kb * 8, h, t0, b, bar_in);
+  };
+  if (tid == 0) load_chunk(0);
+  bool in_flight = true;  // a tensor copy into the tiles has been issued and not waited for
+
+  constexpr uint32_t ID_G = idesc(Q, Q, 0, 0);      // C (K-major) x B^T (K-major)
+  constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);     // M or C (K-major) x X or h (MN-major)
+  constexpr uint32_t ID_S = idesc(128, PB, 1, 1);   // B^T (MN-major) x Xw (MN-major)
+
+  uint32_t cur = 0;  // phase parity of the chunk in hand
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const uint32_t par = c & 1;
+    cur = par;
+    const int64_t t0 = (int64_t)c * Q;
+    const int i = tid;  // this thread's row of every Q-row product
+    const bool valid = t0 + i < L;
+    // ---- per-step vectors: step_i, the running sum S_i of step * A (block scan), the
+    // chunk's range of S and the split decay factors
+    float step = 0.f;
+    if (valid) {
+      const float v = __bfloat162float(p.dt[((int64_t)b * L + t0 + i) * p.H + h]) + biash;
+      step = p.softplus ? (v > 20.f ? v : log1pf(expf(v))) : v;
+    }
+    float incl = step * Ah;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    __syncthreads();  // the previous chunk's readers of Sv, stepv, bv and red are done
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) incl += red[w];
+    const float Si = incl;
+    float mn = Si, mx = Si;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (lane == 0) {
+      red[4 + warp] = mn;
+      red[8 + warp] = mx;
+    }
+    Sv[i] = Si;
+    stepv[i] = step;
+    __syncthreads();
+    mn = fminf(fminf(red[4], red[5]), fminf(red[6], red[7]));
+    mx = fmaxf(fmaxf(red[8], red[9]), fmaxf(red[10], red[11]));
+    const float Slast = Sv[Q - 1];
+    // both factors within e^(+-80) (inside fp32) when the range of S is at most 160
+    const bool split = (mx - mn) <= 160.f;
+    const float Sref = 0.5f * (mn + mx);
+    const float ai = ex2f((Si - Sref) * kLog2e);
+    bv[i] = ex2f((Sref - Si) * kLog2e) * step;
+
+    // ---- the chunk's inputs; G = C B^T (every wait is decided by all threads together,
+    // so that they leave the loop at the same point)
+    if (!__syncthreads_and(mbar_wait(bar_in, par))) { ok = false; break; }
+    in_flight = false;
+    if (tid == 0) {
+      tc_fence_after();
+      for (int k = 0; k < kN; ++k)
+        mma(tmem + Sm::T_G, sdesc(s_base + Sm::C_OFF + k * 2 * Q * 16, Q * 16, 128),
+            sdesc(s_base + Sm::B_OFF + k * 2 * Q * 16, Q * 16, 128), ID_G, k > 0);
+      mma_commit(bar_g);
+    }
+    issued |= 1;
+
+    // ---- Xw_j = exp(S_last - S_j) step_j x_j (hi, lo); x_i kept for D x_i; z_i fetched
+    uint32_t xr[PB / 2];
+    uint4 zv[PB / 8];
+#pragma unroll
+    for (int q = 0; q < PB / 8; ++q) zv[q] = make_uint4(0, 0, 0, 0);
+    const int64_t row = (((int64_t)b * L + t0 + i) * p.H + h) * P + pc;
+    if (p.z && valid) {
+#pragma unroll
+      for (int q = 0; q < PB / 8; ++q) zv[q] = __ldg(reinterpret_cast<const uint4*>(p.z + row) + q);
+    }
+    {
+      const float wj = ex2f((Slast - Si) * kLog2e) * step;
+#pragma unroll
+      for (int cb = 0; cb < PB / 8; ++cb) {
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + Sm::X_OFF + cm(i, cb, Q));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xr[cb * 4 + e] = w[e];
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          split2(f.x * wj, f.y * wj, hi[e], lo[e]);
+        }
+        *reinterpret_cast<uint4*>(smem + Sm::W_OFF + cm(i, cb, Q)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + Sm::W_OFF + Q * PB * 2 + cm(i, cb, Q)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    // ---- the state: its bf16 copy (hi, lo) for C h_prev, then h <- exp(S_last) h
+    {
+      const float dl = ex2f(Slast * kLog2e);
+#pragma unroll 1
+      for (int nb = 0; nb < NP / 128; ++nb) {
+        const int n = nb * 128 + i;
+#pragma unroll 1
+        for (int c0 = 0; c0 < PB; c0 += 32) {
+          float v[32];
+          tmem_ld32(lane_t + Sm::T_H + nb * PB + c0, v);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split2(v[cb * 8 + 2 * e], v[cb * 8 + 2 * e + 1], hi[e], lo[e]);
+            const uint32_t off = cm(n, (c0 >> 3) + cb, NP);
+            *reinterpret_cast<uint4*>(smem + Sm::H_OFF + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + Sm::H_OFF + NP * PB * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= dl;
+          tmem_st32(lane_t + Sm::T_H + nb * PB + c0, v);
+        }
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    // ---- Yo = C h_prev (hi + lo); h += B^T Xw (hi + lo)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      for (int part = 0; part < 2; ++part)
+        for (int k = 0; k < kN; ++k)  // C (K-major, K = n) x state (MN-major)
+          mma(tmem + Sm::T_YO, sdesc(s_base + Sm::C_OFF + k * 2 * Q * 16, Q * 16, 128),
+              sdesc(s_base + Sm::H_OFF + part * NP * PB * 2 + k * 256, 128, NP * 16), ID_Y, part > 0 || k > 0);
+      for (int nb = 0; nb < NP / 128; ++nb)
+        for (int part = 0; part < 2; ++part)
+          for (int k = 0; k < Q / 16; ++k)  // B^T (MN-major: M = n, K = j) x Xw (MN-major)
+            mma(tmem + Sm::T_H + nb * PB, sdesc(s_base + Sm::B_OFF + nb * 16 * Q * 16 + k * 256, 128, Q * 16),
+                sdesc(s_base + Sm::W_OFF + part * Q * PB * 2 + k * 256, 128, Q * 16), ID_S, true);
+      mma_commit(bar_s);
+    }
+    issued |= 2;
+
+    // ---- M[i][j] = G[i][j] exp(S_i - S_j) step_j (j <= i), hi + lo, over the space of C
+    // and B once the products reading them are done
+    if (!__syncthreads_and(mbar_wait(bar_g, par))) { ok = false; break; }
+    issued &= ~1;
+    tc_fence_after();
+#pragma unroll 1
+    for (int J = 0; J < Q / 32; ++J) {
+      const int j0 = J * 32;
+      uint32_t hi[16], lo[16];
+      if (J <= warp) {  // warp-uniform: blocks right of the diagonal block are zero
+        float gv[32];
+        tmem_ld32(lane_t + Sm::T_G + j0, gv);
+        float m[32];
+        if (split) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bv + j0 + 4 * q);
+            m[4 * q + 0] = gv[4 * q + 0] * (ai * b4.x);
+            m[4 * q + 1] = gv[4 * q + 1] * (ai * b4.y);
+            m[4 * q + 2] = gv[4 * q + 2] * (ai * b4.z);
+            m[4 * q + 3] = gv[4 * q + 3] * (ai * b4.w);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) m[jj] = gv[jj] * ex2f((Si - Sv[j0 + jj]) * kLog2e) * stepv[j0 + jj];
+        }
+        if (J == warp) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) m[jj] = (j0 + jj <= i) ? m[jj] : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split2(m[2 * e], m[2 * e + 1], hi[e], lo[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+      }
+      if (J == 0) {
+        if (!__syncthreads_and(mbar_wait(bar_s, par))) ok = false;
+        tc_fence_after();
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        const uint32_t off = cm(i, J * 4 + cb, Q);
+        *reinterpret_cast<uint4*>(smem + Sm::M_OFF + off) =
+            make_uint4(hi[4 * cb], hi[4 * cb + 1], hi[4 * cb + 2], hi[4 * cb + 3]);
+        *reinterpret_cast<uint4*>(smem + Sm::M_OFF + Q * Q * 2 + off) =
+            make_uint4(lo[4 * cb], lo[4 * cb + 1], lo[4 * cb + 2], lo[4 * cb + 3]);
+      }
+    }
+    if (!ok) break;
+    issued &= ~2;
+    // ---- Yd = M X (hi + lo)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      for (int part = 0; part < 2; ++part)
+        for (int k = 0; k < Q / 16; ++k)  // M (K-major, K = j) x X (MN-major)
+          mma(tmem + Sm::T_YD, sdesc(s_base + Sm::M_OFF + part * Q * Q * 2 + k * 2 * Q * 16, Q * 16, 128),
+              sdesc(s_base + Sm::X_OFF + k * 256, 128, Q * 16), ID_Y, part > 0 || k > 0);
+      mma_commit(bar_y);
+    }
+    issued |= 4;
+    if (!__syncthreads_and(mbar_wait(bar_y, par))) { ok = false; break; }
+    issued &= ~4;
+    tc_fence_after();
+    // the tiles are consumed: fetch the next chunk's inputs while the outputs are formed
+    if (c + 1 < nch) {
+      if (tid == 0) load_chunk(c + 1);
+      in_flight = true;
+    }
+
+    // ---- y = Yd + exp(S_i) Yo + D x; out = y silu(z).  The tensor-memory loads are
+    // warp-wide (.sync.aligned): every lane takes them, only valid rows store.
+    {
+      const float ei = ex2f(Si * kLog2e);
+#pragma unroll
+      for (int c0 = 0; c0 < PB; c0 += 32) {
+        float yd[32], yo[32];
+        tmem_ld32(lane_t + Sm::T_YD + c0, yd);
+        tmem_ld32(lane_t + Sm::T_YO + c0, yo);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[4];
+          const uint4 zq = p.z ? zv[(c0 >> 3) + q] : make_uint4(0, 0, 0, 0);
+          const uint32_t zw[4] = {zq.x, zq.y, zq.z, zq.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = q * 8 + 2 * e;
+            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr[(c0 + j) / 2]));
+            float y0 = fmaf(Dh, xf.x, fmaf(ei, yo[j], yd[j]));
+            float y1 = fmaf(Dh, xf.y, fmaf(ei, yo[j + 1], yd[j + 1]));
+            if (p.z) {
+              const float2 zf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw[e]));
+              y0 *= __fdividef(zf.x, 1.f + ex2f(-zf.x * kLog2e));
+              y1 *= __fdividef(zf.y, 1.f + ex2f(-zf.y * kLog2e));
+            }
+            o[e] = pack2(y0, y1);
+          }
+          if (valid) reinterpret_cast<uint4*>(p.out + row + c0)[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  if (!ok && tid == 0) atomicExch(p.status, 1);
+
+  // the final state: lane n, columns of PB channels -> state[b, h, pc + j, n]
+  if (ok && p.state) {
+    const int64_t sb = ((int64_t)b * p.H + h) * P * N;
+#pragma unroll 1
+    for (int nb = 0; nb < NP / 128; ++nb) {
+      const int n = nb * 128 + tid;
+#pragma unroll 1
+      for (int c0 = 0; c0 < PB; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_t + Sm::T_H + nb * PB + c0, v);
+        if (n < N)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) p.state[sb + (int64_t)(pc + c0 + j) * N + n] = v[j];
+      }
+    }
+  }
+  // after a wait that ran out, let the tensor copy and the products still in flight
+  // finish (each wait bounded) before the shared and tensor memory are released
+  if (!ok && tid == 0) {  // everything outstanding belongs to the chunk the loop left at
+    if (in_flight) mbar_wait(bar_in, cur);
+    if (issued & 1) mbar_wait(bar_g, cur);
+    if (issued & 2) mbar_wait(bar_s, cur);
+    if (issued & 4) mbar_wait(bar_y, cur);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Sm::TCOLS) : "memory");
+}
+
+}  // namespace ssd

@@ -383,6 +383,12 @@ namespace ssm_internal {
 
 void count_launch() { g_launches.fetch_add(1); }
 
+int* status_word() {
+  int* status = nullptr;
+  if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return nullptr;
+  return status;
+}
+
 // The whole call.  scratch == nullptr: the chunk-carry workspace comes from the
 // library's stream-ordered pool.  Otherwise it is carved from `scratch`
 // (scratch_bytes long, device memory the caller keeps), nothing is allocated, and a
@@ -821,7 +827,7 @@ int ssm_set_option(const char* name, int64_t value) {
   else if (!std::strcmp(name, "inject_stall")) g_opt_inject_stall = std::min<int64_t>(value, INT32_MAX);
   else if (!std::strcmp(name, "one_launch")) g_opt_one_launch = value ? 1 : 0;
   else if (!std::strcmp(name, "hold_chunk")) g_opt_hold_chunk = std::min<int64_t>(value, INT32_MAX);
-  else return SSM_ERR_DIMS;
+  else if (!ssm_internal::set_ssd_option(name, value)) return SSM_ERR_DIMS;
   return SSM_OK;
 }
 

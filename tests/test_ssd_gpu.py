@@ -3,8 +3,8 @@
 Outputs and the final state are compared element by element with the floored
 relative error at the bf16 bar (2e-2): inputs are bf16, and the kernel's tensor
 core operands (the masked decay matrix, the decay-weighted inputs, the carried
-state) are bf16 with fp32 accumulation.  Sizes span several 64-step chunks and
-ragged tails; the full-size layer is checked on sampled heads.
+state) are pairs of bf16 values with fp32 accumulation.  Sizes span several 128-step
+chunks and ragged tails; the full-size layer is checked on sampled heads.
 """
 import zlib
 
@@ -28,6 +28,7 @@ def ssd_gpu(w, h0=None):
     o, f = ssm.ssm_ssd_fwd(to_torch(w.x), to_torch(w.dt), to_torch(w.A), to_torch(w.B), to_torch(w.C),
                            to_torch(w.D), to_torch(w.z), to_torch(w.dt_bias), final_state=fs,
                            dt_softplus=w.dt_softplus, state_in=h0 is not None)
+    assert ssm.ssm_check_status() == 0
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), f.cpu().numpy().astype(np.float64)
 
@@ -75,6 +76,20 @@ def test_ssd_without_softplus():
     ref, ref_st = ssd_oracle(w)
     assert_close(out, ref, "bf16", "no softplus: out")
     assert_close(st, ref_st, "bf16", "no softplus: final state")
+
+
+def test_ssd_fast_decay_takes_the_unsplit_path():
+    """Large steps on a fast-decaying head: a chunk's range of S (the running sum of
+    step * A) far above 160, where the kernel forms each decay exp(S_i - S_j) with its
+    own exponential instead of the split product; most decays underflow to zero."""
+    w = make_ssd("fast", batch=1, seqlen=300, nheads=3, headdim=64, dstate=128, seed=8,
+                 state_in=True)
+    w.dt_bias = np.full(w.nheads, 2.0, np.float32)          # steps near 2
+    w.A = np.array([-1.5, -0.05, -3.0], np.float32)          # ranges ~380, ~13, ~770 per chunk
+    out, st = ssd_gpu(w)
+    ref, ref_st = ssd_oracle(w)
+    assert_close(out, ref, "bf16", "fast decay: out")
+    assert_close(st, ref_st, "bf16", "fast decay: final state")
 
 
 def test_ssd_continuation_and_determinism():
