@@ -523,17 +523,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A (inner, mid, L, batch) bf16 tensor, boxes of 8 inner values x 1 x Q steps x 1: one
-// block of 8 columns of a chunk, laid out as Q rows of 16 bytes.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch) {
+// A (batch, L, mid, inner) bf16 tensor seen as 5-D: (8 values, L rows, inner / 8
+// blocks of 8 values, mid, batch).  A box of (8, Q, blocks, 1, 1) lands in shared memory
+// block by block, each block Q rows of 16 bytes: the no-swizzle core-matrix layout of
+// the tensor-core operands.
+bool encode_tile(CUtensorMap* m, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch,
+                 int blocks) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2),
+  const cuuint64_t dims[5] = {8, (cuuint64_t)L, (cuuint64_t)(inner / 8), (cuuint64_t)mid, (cuuint64_t)batch};
+  const cuuint64_t strides[4] = {(cuuint64_t)(inner * mid * 2), 16, (cuuint64_t)(inner * 2),
                                  (cuuint64_t)(inner * mid * L * 2)};
-  const cuuint32_t box[4] = {8, 1, (cuuint32_t)ssd::Q, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint32_t box[5] = {8, (cuuint32_t)ssd::Q, (cuuint32_t)blocks, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -553,9 +556,9 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t strea
   }
   ssd::Maps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (!encode_rows(&maps.x, prm.x, P, prm.H, prm.L, batch) ||
-      !encode_rows(&maps.B, prm.B, N, prm.G, prm.L, batch) ||
-      !encode_rows(&maps.C, prm.C, N, prm.G, prm.L, batch))
+  if (!encode_tile(&maps.x, prm.x, P, prm.H, prm.L, batch, PB / 8) ||
+      !encode_tile(&maps.B, prm.B, N, prm.G, prm.L, batch, N / 8) ||
+      !encode_tile(&maps.C, prm.C, N, prm.G, prm.L, batch, N / 8))
     return SSM_ERR_CUDA;
   ssd::Params p;
   std::memset(&p, 0, sizeof p);

@@ -18,9 +18,13 @@
 // TMEM), issued by one thread and completed on mbarriers.  Operands sit in shared
 // memory in the no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix,
 // blocks of 8 columns stored one after another): C, B and x arrive that way by TMA
-// tensor copies (one box of 8 columns x Q rows per block); M, Xw and the state copy
-// are written there by the threads.  Thread i owns TMEM lane i (row i of every
-// accumulator) for the element-wise work.
+// tensor copies (one 5-D box per tensor and chunk, whose dimensions -- 8 columns, Q
+// rows, the blocks of 8 columns -- lay the tile out block by block); M, Xw and the
+// state copy are written there by the threads.  Thread i owns TMEM lane i (row i of
+// every accumulator) for the element-wise work.  A value held as a pair of bf16 parts
+// enters a product as one operand twice as wide (parts side by side), so that one
+// instruction forms both partial products into adjacent accumulator columns; the
+// carried state is held as two accumulators (the sum so far, this chunk's low parts).
 //
 // Order inside a chunk: G is issued as soon as the inputs land; while it runs the
 // threads form Xw and the state copy, then C h_prev and B^T Xw are issued; M is formed
@@ -51,9 +55,11 @@ constexpr int P = 64;       // channels per head
 constexpr int NTHR = 128;   // threads per CTA: one per TMEM lane
 constexpr uint64_t kWaitNs = 2000000000ull;
 
+// 5-D tensor maps (8 columns, L rows, blocks of 8 columns, head or group, batch row):
+// one box of (8, Q, blocks, 1, 1) is a chunk's tile in the core-matrix layout.
 struct Maps {
-  CUtensorMap x;   // (P, H, L, batch), box (8, 1, Q, 1)
-  CUtensorMap B;   // (N, G, L, batch), box (8, 1, Q, 1)
+  CUtensorMap x;   // box (8, Q, PB / 8, 1, 1)
+  CUtensorMap B;   // box (8, Q, N / 8, 1, 1)
   CUtensorMap C;
 };
 
@@ -85,9 +91,11 @@ struct Smem {
   static constexpr int V_OFF = H_OFF + 2 * NP * PB * 2;  // S, step, b (Q floats each), reductions
   static constexpr int BAR_OFF = V_OFF + 3 * Q * 4 + 64;
   static constexpr int BYTES = BAR_OFF + 64;
-  // TMEM columns: G, Yd, Yo, state (NP / 128 blocks of PB)
-  static constexpr int T_G = 0, T_YD = Q, T_YO = Q + PB, T_H = Q + 2 * PB;
-  static constexpr int TUSED = T_H + (NP / 128) * PB;
+  // TMEM columns: G (then M_hi X and M_lo X in its first 2 PB columns), C h_hi | C h_lo,
+  // and per 128 state rows the state's two accumulators (sum so far | low parts)
+  static constexpr int T_G = 0, T_YO = Q, T_H = Q + 2 * PB;
+  static constexpr int TUSED = T_H + (NP / 128) * 2 * PB;
+  static_assert(2 * PB <= Q, "the products M X fit in the columns of G");
   static constexpr int TCOLS = TUSED <= 256 ? 256 : 512;
   static_assert(TUSED <= 512, "tensor memory columns");
   static_assert(2 * Q * Q * 2 <= X_OFF, "M (hi, lo) fits in the space of C and B");
@@ -159,9 +167,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 consecutive fp32 columns of this thread's lane; the load's wait is the caller's
+// (tmem_wait_ld on each destination) so that several loads are in flight together.
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -171,7 +179,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Wait for this thread's tensor-memory loads; the registers of r pass through the
+// statement so that no use of them is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, waited for.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld32_nw(taddr, r);
+  tmem_wait_ld(r);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
@@ -194,12 +221,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
 
@@ -228,7 +255,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __device__ __forceinline__ uint32_t cm(int r, int cb, int R) { return (uint32_t)(cb * R + r) * 16u; }
 
 template <int NP, int PB>
-__global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 1)
+__global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::TCOLS <= 256) ? 2 : 1)
     ssd_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
   using Sm = Smem<NP, PB>;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -272,7 +299,8 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
   bool ok = true;
   int issued = 0;  // products issued and not yet waited for: bit 0 G, 1 C h / B^T Xw, 2 M X
 
-  // the state: h_{-1} (or zeros) into TMEM, lane n = state n, columns of PB channels
+  // the state: h_{-1} (or zeros) into its first accumulator, zeros into the second;
+  // lane n = state n, columns of PB channels
   {
     const int64_t sb = ((int64_t)b * p.H + h) * P * N;
 #pragma unroll 1
@@ -280,35 +308,48 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
       const int n = nb * 128 + tid;
 #pragma unroll 1
       for (int c0 = 0; c0 < PB; c0 += 32) {
-        float v[32];
+        float v[32], zero[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 32; ++j) {
           v[j] = (p.state_in && n < N) ? p.state[sb + (int64_t)(pc + c0 + j) * N + n] : 0.f;
-        tmem_st32(lane_t + Sm::T_H + nb * PB + c0, v);
+          zero[j] = 0.f;
+        }
+        tmem_st32(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
+        tmem_st32(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, zero);
       }
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   }
 
-  // the inputs of chunk c: C, B (N / 8 column blocks) and x (PB / 8 blocks) by TMA
+  // the inputs of chunk c: C, B (Q x N) and x (Q x PB), one tensor copy each
   const uint32_t in_bytes = (uint32_t)((2 * (N / 8) + PB / 8) * Q * 16);
   auto load_chunk = [&](int c) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_in), "r"(in_bytes)
                  : "memory");
     const int t0 = c * Q;
-    for (int kb = 0; kb < N / 8; ++kb) {
-      tma_load_4d(s_base + Sm::C_OFF + kb * Q * 16, &maps.C, kb * 8, g, t0, b, bar_in);
-      tma_load_4d(s_base + Sm::B_OFF + kb * Q * 16, &maps.B, kb * 8, g, t0, b, bar_in);
-    }
-    for (int kb = 0; kb < PB / 8; ++kb)
-      tma_load_4d(s_base + Sm::X_OFF + kb * Q * 16, &maps.x, pc + kb * 8, h, t0, b, bar_in);
+    tma_load_5d(s_base + Sm::C_OFF, &maps.C, 0, t0, 0, g, b, bar_in);
+    tma_load_5d(s_base + Sm::B_OFF, &maps.B, 0, t0, 0, g, b, bar_in);
+    tma_load_5d(s_base + Sm::X_OFF, &maps.x, 0, t0, pc / 8, h, b, bar_in);
   };
   if (tid == 0) load_chunk(0);
   bool in_flight = true;  // a tensor copy into the tiles has been issued and not waited for
 
-  constexpr uint32_t ID_G = idesc(Q, Q, 0, 0);      // C (K-major) x B^T (K-major)
-  constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);     // M or C (K-major) x X or h (MN-major)
-  constexpr uint32_t ID_S = idesc(128, PB, 1, 1);   // B^T (MN-major) x Xw (MN-major)
+  constexpr uint32_t ID_G = idesc(Q, Q, 0, 0);          // C (K-major) x B^T (K-major)
+  constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);         // M (K-major) x X (MN-major)
+  constexpr uint32_t ID_O = idesc(Q, 2 * PB, 0, 1);     // C (K-major) x [h_hi | h_lo] (MN-major)
+  constexpr uint32_t ID_S = idesc(128, 2 * PB, 1, 1);   // B^T (MN-major) x [Xw_hi | Xw_lo] (MN-major)
+  // operand descriptors at offset 0; a K step adds its byte offset / 16
+  const uint64_t dC = sdesc(s_base + Sm::C_OFF, Q * 16, 128);    // K-major, K = n
+  const uint64_t dB = sdesc(s_base + Sm::B_OFF, Q * 16, 128);    // K-major, K = n
+  const uint64_t dBt = sdesc(s_base + Sm::B_OFF, 128, Q * 16);   // MN-major: M = n, K = j
+  const uint64_t dH = sdesc(s_base + Sm::H_OFF, 128, NP * 16);   // MN-major: N = channel, K = n
+  const uint64_t dW = sdesc(s_base + Sm::W_OFF, 128, Q * 16);    // MN-major: N = channel, K = j
+  const uint64_t dM = sdesc(s_base + Sm::M_OFF, Q * 16, 128);    // K-major, K = j
+  const uint64_t dX = sdesc(s_base + Sm::X_OFF, 128, Q * 16);    // MN-major: N = channel, K = j
+  auto off16 = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
+
+  // the raw step of this thread's row, one chunk ahead
+  float dt_next = (tid < L) ? __bfloat162float(p.dt[((int64_t)b * L + tid) * p.H + h]) : 0.f;
 
   uint32_t cur = 0;  // phase parity of the chunk in hand
 #pragma unroll 1
@@ -320,9 +361,11 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
     const bool valid = t0 + i < L;
     // ---- per-step vectors: step_i, the running sum S_i of step * A (block scan), the
     // chunk's range of S and the split decay factors
+    const float dt_raw = dt_next;
+    dt_next = (t0 + Q + i < L) ? __bfloat162float(p.dt[((int64_t)b * L + t0 + Q + i) * p.H + h]) : 0.f;
     float step = 0.f;
     if (valid) {
-      const float v = __bfloat162float(p.dt[((int64_t)b * L + t0 + i) * p.H + h]) + biash;
+      const float v = dt_raw + biash;
       step = p.softplus ? (v > 20.f ? v : log1pf(expf(v))) : v;
     }
     float incl = step * Ah;
@@ -365,8 +408,7 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
     if (tid == 0) {
       tc_fence_after();
       for (int k = 0; k < kN; ++k)
-        mma(tmem + Sm::T_G, sdesc(s_base + Sm::C_OFF + k * 2 * Q * 16, Q * 16, 128),
-            sdesc(s_base + Sm::B_OFF + k * 2 * Q * 16, Q * 16, 128), ID_G, k > 0);
+        mma(tmem + Sm::T_G, dC + off16(k * 2 * Q * 16), dB + off16(k * 2 * Q * 16), ID_G, k > 0);
       mma_commit(bar_g);
     }
     issued |= 1;
@@ -399,7 +441,8 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
-    // ---- the state: its bf16 copy (hi, lo) for C h_prev, then h <- exp(S_last) h
+    // ---- the state (sum of its two accumulators): its bf16 copy (hi, lo) for C h_prev,
+    // then h <- exp(S_last) h into the first accumulator, zeros into the second
     {
       const float dl = ex2f(Slast * kLog2e);
 #pragma unroll 1
@@ -407,8 +450,18 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
         const int n = nb * 128 + i;
 #pragma unroll 1
         for (int c0 = 0; c0 < PB; c0 += 32) {
-          float v[32];
-          tmem_ld32(lane_t + Sm::T_H + nb * PB + c0, v);
+          const uint32_t ta = lane_t + Sm::T_H + nb * 2 * PB + c0;
+          uint32_t ra[32], rb[32];
+          tmem_ld32_nw(ta, ra);
+          tmem_ld32_nw(ta + PB, rb);
+          tmem_wait_ld(ra);
+          tmem_wait_ld(rb);
+          float v[32], zero[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+            zero[j] = 0.f;
+          }
 #pragma unroll
           for (int cb = 0; cb < 4; ++cb) {
             uint32_t hi[4], lo[4];
@@ -420,7 +473,8 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= dl;
-          tmem_st32(lane_t + Sm::T_H + nb * PB + c0, v);
+          tmem_st32(ta, v);
+          tmem_st32(ta + PB, zero);
         }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -431,15 +485,15 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      for (int part = 0; part < 2; ++part)
-        for (int k = 0; k < kN; ++k)  // C (K-major, K = n) x state (MN-major)
-          mma(tmem + Sm::T_YO, sdesc(s_base + Sm::C_OFF + k * 2 * Q * 16, Q * 16, 128),
-              sdesc(s_base + Sm::H_OFF + part * NP * PB * 2 + k * 256, 128, NP * 16), ID_Y, part > 0 || k > 0);
-      for (int nb = 0; nb < NP / 128; ++nb)
-        for (int part = 0; part < 2; ++part)
-          for (int k = 0; k < Q / 16; ++k)  // B^T (MN-major: M = n, K = j) x Xw (MN-major)
-            mma(tmem + Sm::T_H + nb * PB, sdesc(s_base + Sm::B_OFF + nb * 16 * Q * 16 + k * 256, 128, Q * 16),
-                sdesc(s_base + Sm::W_OFF + part * Q * PB * 2 + k * 256, 128, Q * 16), ID_S, true);
+      // the two chains interleaved: C h_prev (K = n) and, per 128 state rows, B^T Xw (K = j)
+      const int kmax = kN > Q / 16 ? kN : Q / 16;
+      for (int k = 0; k < kmax; ++k) {
+        if (k < kN) mma(tmem + Sm::T_YO, dC + off16(k * 2 * Q * 16), dH + off16(k * 256), ID_O, k > 0);
+        if (k < Q / 16)
+          for (int nb = 0; nb < NP / 128; ++nb)
+            mma(tmem + Sm::T_H + nb * 2 * PB, dBt + off16(nb * 16 * Q * 16 + k * 256), dW + off16(k * 256), ID_S,
+                true);
+      }
       mma_commit(bar_s);
     }
     issued |= 2;
@@ -502,10 +556,10 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      for (int part = 0; part < 2; ++part)
-        for (int k = 0; k < Q / 16; ++k)  // M (K-major, K = j) x X (MN-major)
-          mma(tmem + Sm::T_YD, sdesc(s_base + Sm::M_OFF + part * Q * Q * 2 + k * 2 * Q * 16, Q * 16, 128),
-              sdesc(s_base + Sm::X_OFF + k * 256, 128, Q * 16), ID_Y, part > 0 || k > 0);
+      for (int k = 0; k < Q / 16; ++k) {  // M_hi X and M_lo X, two chains in the columns of G
+        mma(tmem + Sm::T_G, dM + off16(k * 2 * Q * 16), dX + off16(k * 256), ID_Y, k > 0);
+        mma(tmem + Sm::T_G + PB, dM + off16(Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 256), ID_Y, k > 0);
+      }
       mma_commit(bar_y);
     }
     issued |= 4;
@@ -525,8 +579,21 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
 #pragma unroll
       for (int c0 = 0; c0 < PB; c0 += 32) {
         float yd[32], yo[32];
-        tmem_ld32(lane_t + Sm::T_YD + c0, yd);
-        tmem_ld32(lane_t + Sm::T_YO + c0, yo);
+        {
+          uint32_t ra[32], rb[32];
+          tmem_ld32_nw(lane_t + Sm::T_G + c0, ra);
+          tmem_ld32_nw(lane_t + Sm::T_G + PB + c0, rb);
+          tmem_wait_ld(ra);
+          tmem_wait_ld(rb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) yd[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+          tmem_ld32_nw(lane_t + Sm::T_YO + c0, ra);
+          tmem_ld32_nw(lane_t + Sm::T_YO + PB + c0, rb);
+          tmem_wait_ld(ra);
+          tmem_wait_ld(rb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) yo[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t o[4];
@@ -561,8 +628,11 @@ __global__ void __launch_bounds__(NTHR, Smem<NP, PB>::BYTES <= 110 * 1024 ? 2 : 
       const int n = nb * 128 + tid;
 #pragma unroll 1
       for (int c0 = 0; c0 < PB; c0 += 32) {
-        float v[32];
-        tmem_ld32(lane_t + Sm::T_H + nb * PB + c0, v);
+        float v[32], w2[32];
+        tmem_ld32(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
+        tmem_ld32(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, w2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += w2[j];
         if (n < N)
 #pragma unroll
           for (int j = 0; j < 32; ++j) p.state[sb + (int64_t)(pc + c0 + j) * N + n] = v[j];
