@@ -43,10 +43,10 @@ UPDATES_PER_SM_CLK = min(EX2_PER_SM_CLK, FMA_LANES_PER_SM_CLK / FMA_OPS_PER_UPDA
 # its kernel launches), from one ncu capture, with the sha256 of the kernel sources it
 # was taken on; reported as null once the sources change.  See profiles/.
 TRAFFIC = {
-    # long_bf16_16k capture (aggregate launch 167.4 MB + output launch 315.5 MB, means
+    # long_bf16_16k capture (aggregate launch 166.6 MB + output launch 315.6 MB, means
     # of 5), scaled by the units processed (x8) to the 131072-step workload
-    "long_bf16": {"bytes_per_call": 3863000000, "kernel_src_sha": "ee3f4713096a6f8e"},
-    "long_bf16_16k": {"bytes_per_call": 482900000, "kernel_src_sha": "ee3f4713096a6f8e"},
+    "long_bf16": {"bytes_per_call": 3857600000, "kernel_src_sha": "30a783e390386982"},
+    "long_bf16_16k": {"bytes_per_call": 482200000, "kernel_src_sha": "30a783e390386982"},
 }
 
 
@@ -373,6 +373,106 @@ def other_workloads(torch, ssm, device, names, reps=20):
     return out
 
 
+def ssd_and_backward_configs(torch, ssm, device, main_w=None, main_t=None, reps=10):
+    """The Mamba-2 SSD layers and the backward pass of the long-context layer, timed in
+    the same run as the headline (median of `reps` calls; inputs larger than L2), so
+    that their figures appear in the line: per call the time, the HBM fraction of the
+    algorithmic bytes and, for SSD, the tensor fraction of its flops; for the backward
+    the split over its kernels and the fraction of its MUFU bound.  The headline's
+    tensors are reused when it is the long-context layer (same seed on rank 0)."""
+    from selective_state_space_112_b300.workloads import (SSD_CONFIGS, config, f32_to_bf16_bits,
+                                                          make_ssd)
+    stream = torch.cuda.current_stream(device)
+    hbm_peak, sm_max, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc_peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        tc_peak = 1800.0
+    out = {}
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    for name in ("mamba2_2p7b_bf16", "mamba2_n256_bf16"):
+        w = make_ssd(name, **SSD_CONFIGS[name])
+        t = {k: (None if getattr(w, k) is None else
+                 (bf(getattr(w, k)) if getattr(w, k).dtype == np.uint16 else
+                  torch.from_numpy(getattr(w, k))).to(device))
+             for k in ("x", "dt", "A", "B", "C", "D", "z", "dt_bias")}
+        o = torch.empty_like(t["x"])
+        fs = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=device)
+
+        def call():
+            ssm.ssm_ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["z"], t["dt_bias"],
+                            out=o, final_state=fs)
+        for _ in range(3):
+            call()
+        assert ssm.ssm_check_status() == 0
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            times = sorted(timed_calls(call, torch, stream, reps))
+        assert ssm.ssm_check_status() == 0
+        med = statistics.median(times)
+        byt, flops = ssd_algorithmic(w)
+        out["ssd_" + name] = {
+            "layer": "Mamba-2 SSD", "kernel": "ssd_tc_kernel",
+            "shape": {"batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+                      "dstate": w.dstate, "ngroups": w.ngroups},
+            "ms_median": round(med, 5), "ms_min": round(times[0], 5),
+            "tokens_channels_per_s": w.tokens_channels / (med * 1e-3),
+            "hbm": {"achieved": round(byt / (med * 1e-3) / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(byt / (med * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": peak_kind},
+            "tensor": {"achieved": round(flops / (med * 1e-3) / 1e12, 2), "peak": tc_peak,
+                       "unit": "TFLOP/s", "frac": round(flops / (med * 1e-3) / 1e12 / tc_peak, 4)},
+            "reps": reps, "clocks": clk.summary()}
+        del t, o, fs
+        torch.cuda.empty_cache()
+    # the backward pass of the long-context layer
+    if main_w is not None and main_w.name == "long_bf16":
+        w, t = main_w, main_t
+    else:
+        w = config("long_bf16")
+        t = device_tensors(w, torch, device)
+    rng = np.random.default_rng(w.seed + 4242)
+    dout = bf(f32_to_bf16_bits(rng.standard_normal(w.x.shape, dtype=np.float32))).to(device)
+    grads = ssm.ssm_selective_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                       t["delta_bias"], t["h0"], dout, delta_softplus=w.delta_softplus)
+
+    def bwd():
+        ssm.ssm_selective_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                   t["delta_bias"], t["h0"], dout, delta_softplus=w.delta_softplus,
+                                   grads=grads)
+    for _ in range(3):
+        bwd()
+    assert ssm.ssm_check_status() == 0
+    ssm.ssm_profile_enable(True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        times = sorted(timed_calls(bwd, torch, stream, max(3, reps // 2)))
+    ssm.ssm_profile_enable(False)
+    prof = ssm.ssm_profile_read()
+    assert ssm.ssm_check_status() == 0
+    med = statistics.median(times)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    dom = max(prof, key=lambda k: prof[k][1]) if prof else None
+    dom_ms = prof[dom][1] / prof[dom][0] if dom else med
+    upd_peak = EX2_PER_SM_CLK / BWD_EX2_PER_UPDATE * sms * sm_max * 1e6 / 1e9
+    esz = 2
+    alg = (w.tokens_channels * esz * 7 + w.batch * w.seqlen * w.dstate * (2 * esz + 8)
+           + w.dim * (w.dstate + 2) * 8)
+    out["backward_long_bf16"] = {
+        "pass": "backward (gradients of every input, states rebuilt from checkpoints)",
+        "shape": {"batch": w.batch, "seqlen": w.seqlen, "dim": w.dim, "dstate": w.dstate},
+        "ms_median": round(med, 4), "ms_min": round(times[0], 4),
+        "hbm": {"achieved": round(alg / (med * 1e-3) / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(alg / (med * 1e-3) / 1e9 / hbm_peak, 4)},
+        "alu": {"kernel": dom, "achieved": round(w.element_updates / (dom_ms * 1e-3) / 1e9, 1),
+                "peak": round(upd_peak, 1), "unit": "Gupdate/s",
+                "frac": round(w.element_updates / (dom_ms * 1e-3) / 1e9 / upd_peak, 4),
+                "peak_basis": f"{EX2_PER_SM_CLK} ex2 / SM / clock / {BWD_EX2_PER_UPDATE} ex2 per update"},
+        "kernels": {k: {"launches": v[0], "ms_avg": round(v[1] / v[0], 4)} for k, v in prof.items()},
+        "clocks": clk.summary()}
+    del grads, dout
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -552,6 +652,7 @@ def main():
         others = [n for n in ("mamba130m_f32", "mamba1p4b_bf16", "step_bf16", "lti_f32", "tiny_f32")
                   if n != args.workload]
         res["configs"] = other_workloads(torch, ssm, device, others)
+        res["configs"].update(ssd_and_backward_configs(torch, ssm, device, w, t))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, cv=cv)
     if world > 1:
@@ -725,14 +826,14 @@ def cpu_baseline_bwd(w, dout, budget_s: float = 15.0):
                       f"({units} tokens*channels, {t:.1f} s, float64 C + OpenMP)"}
 
 
-SSD_Q = 64  # chunk length of the SSD kernel's dual form
+SSD_Q = 128  # chunk length of the SSD kernel's dual form
 
 
 def ssd_algorithmic(w):
     """Bytes and multiply-add flops one SSD call must move / do at least.
     Bytes: x, z in and out once (b L H P, bf16), dt (b L H), B and C (b L G N), the
     per-head parameters and the final state (b H P N fp32).  Flops: the dual form per
-    64-step chunk and head: the causal half of C B^T (Q(Q+1)/2 N) and of M x
+    128-step chunk and head: the causal half of C B^T (Q(Q+1)/2 N) and of M x
     (Q(Q+1)/2 P), the readout of the carried state C h (Q P N) and its update B^T x
     (N P Q), two flops per multiply-add."""
     tc = w.batch * w.seqlen * w.nheads * w.headdim
@@ -811,7 +912,7 @@ def ssd_bench(args, world, rank, local):
     tc_obj = {"bound": "tensor", "achieved": round(tc_ach, 2), "peak": tc_peak, "unit": "TFLOP/s",
               "frac": round(tc_ach / tc_peak, 4), "peak_source": f"{tc_kind} bf16 burst"}
     main_obj, other = (hbm_obj, tc_obj) if t_hbm >= t_tc else (tc_obj, hbm_obj)
-    roof = dict(main_obj, kernel="ssd_fwd_kernel", traffic=None, algorithmic_bytes_per_launch=byt,
+    roof = dict(main_obj, kernel="ssd_tc_kernel", traffic=None, algorithmic_bytes_per_launch=byt,
                 algorithmic_flops_per_launch=flops, kernel_ms_avg=round(ms_step, 4),
                 roofline_ms={"hbm": round(t_hbm * 1e3, 4), "tensor": round(t_tc * 1e3, 4)},
                 other=other)

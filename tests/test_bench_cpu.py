@@ -38,9 +38,10 @@ def test_ssd_algorithmic_counts():
     """Bytes and flops of the 2.7B-shaped SSD layer, counted by hand: x, z, out
     (4 x 4096 x 80 x 64 bf16 each), dt (4 x 4096 x 80 bf16), B and C (4 x 4096 x 128
     bf16 each), A, D, dt_bias (80 fp32 each), the final state (4 x 80 x 64 x 128 fp32);
-    per 64-step chunk and head 2 (64*65/2 (128 + 64) + 2 * 64 * 64 * 128) flops."""
+    per 128-step chunk (32 per sequence) and head 2 (128*129/2 (128 + 64) + 2 * 128 * 64 * 128)
+    flops."""
     import bench
     w = SimpleNamespace(batch=4, seqlen=4096, nheads=80, headdim=64, ngroups=1, dstate=128, z=True)
     byt, flops = bench.ssd_algorithmic(w)
     assert byt == 3 * 167772160 + 2621440 + 2 * 4194304 + 960 + 10485760
-    assert flops == 4 * 80 * 64 * 2 * (2080 * 192 + 2 * 64 * 64 * 128)
+    assert flops == 4 * 80 * 32 * 2 * (8256 * 192 + 2 * 128 * 64 * 128)
