@@ -131,19 +131,16 @@ def test_ssd_empty_sequence():
     assert bool((fs == 3.0).all())
 
 
-def test_ssd_full_size_sampled_heads():
-    """The 2.7B-shaped layer (4 x 4096 steps, 80 heads of 64, N 128) in one call, as
-    the benchmark launches it; sixteen (batch row, head) pairs spread over every batch
-    row and the head range (the first and last head included) against the oracle run
-    on that head's slice of the inputs."""
+def _full_size_sampled(name, npairs, seed):
     import torch
-    cfg = SSD_CONFIGS["mamba2_2p7b_bf16"]
-    w = make_ssd("mamba2_2p7b_bf16", **cfg)
+    cfg = SSD_CONFIGS[name]
+    w = make_ssd(name, **cfg)
     out, st = ssd_gpu(w)
     G = w.ngroups
-    rng = np.random.default_rng(2700)
-    pairs = [(0, 0), (3, 79)] + [(int(b), int(h)) for b, h in
-                                 zip(np.arange(14) % w.batch, rng.choice(w.nheads, 14, replace=False))]
+    rng = np.random.default_rng(seed)
+    pairs = [(0, 0), (w.batch - 1, w.nheads - 1)] + [
+        (int(b), int(h)) for b, h in zip(np.arange(npairs - 2) % w.batch,
+                                         rng.choice(w.nheads, npairs - 2, replace=False))]
     for b, h in pairs:
         g = h // (w.nheads // G)
         sl = make_ssd("slice", batch=1, seqlen=1, nheads=1, headdim=64, dstate=w.dstate, seed=0)
@@ -155,7 +152,22 @@ def test_ssd_full_size_sampled_heads():
         sl.z = w.z[b:b + 1, :, h:h + 1]
         sl.h0 = None
         ref, ref_st = ssd_oracle(sl)
-        assert_close(out[b:b + 1, :, h:h + 1], ref, "bf16", f"full size, b {b} head {h}: out")
-        assert_close(st[b:b + 1, h:h + 1], ref_st, "bf16", f"full size, b {b} head {h}: final state")
+        assert_close(out[b:b + 1, :, h:h + 1], ref, "bf16", f"{name}, b {b} head {h}: out")
+        assert_close(st[b:b + 1, h:h + 1], ref_st, "bf16", f"{name}, b {b} head {h}: final state")
     del out
     torch.cuda.empty_cache()
+
+
+def test_ssd_full_size_sampled_heads():
+    """The 2.7B-shaped layer (4 x 4096 steps, 80 heads of 64, N 128) in one call, as
+    the benchmark launches it; sixteen (batch row, head) pairs spread over every batch
+    row and the head range (the first and last head included) against the oracle run
+    on that head's slice of the inputs."""
+    _full_size_sampled("mamba2_2p7b_bf16", 16, 2700)
+
+
+def test_ssd_full_size_n256_sampled_heads():
+    """The N = 256 layer (4 x 4096 steps, 80 heads of 64) as the benchmark launches it
+    (the kernel for 256 state rows: two blocks of 128 per product), eight (batch row,
+    head) pairs against the oracle."""
+    _full_size_sampled("mamba2_n256_bf16", 8, 2560)
