@@ -27,9 +27,11 @@
 // carried state is held as two accumulators (the sum so far, this chunk's low parts).
 //
 // Order inside a chunk: G is issued as soon as the inputs land; while it runs the
-// threads form Xw and the state copy, then C h_prev and B^T Xw are issued; M is formed
-// from G once those products are done, into the space of C and B (no longer read),
-// and M X is issued last.  The decay factor of M is split as
+// threads form Xw, then C h_prev and B^T Xw are issued; M is formed from G once those
+// products are done, into the space of C and B (no longer read), and M X is issued
+// last.  Then the next chunk's copies are issued, and while they land the threads form
+// the next chunk's per-step vectors and state copy (neither needs its inputs) and this
+// chunk's outputs.  The decay factor of M is split as
 //   exp(S_i - S_j) = exp(S_i - S_ref) exp(S_ref - S_j),  S_ref = the midpoint of the
 // chunk's range of S, so that M costs two multiplies per element; a chunk whose range
 // of S is too wide for both factors to stay inside fp32 takes one exponential per
@@ -351,20 +353,17 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   // the raw step of this thread's row, one chunk ahead
   float dt_next = (tid < L) ? __bfloat162float(p.dt[((int64_t)b * L + tid) * p.H + h]) : 0.f;
 
-  uint32_t cur = 0;  // phase parity of the chunk in hand
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    const uint32_t par = c & 1;
-    cur = par;
+  // ---- per-step vectors of chunk c: step_i, the running sum S_i of step * A (block
+  // scan), the chunk's range of S and the split decay factors (smem: Sv, stepv, bv)
+  const int i = tid;  // this thread's row of every Q-row product, and its state row
+  float step = 0.f, Si = 0.f, Slast = 0.f, ai = 0.f;
+  bool split = true;
+  auto scan = [&](int c) {
     const int64_t t0 = (int64_t)c * Q;
-    const int i = tid;  // this thread's row of every Q-row product
-    const bool valid = t0 + i < L;
-    // ---- per-step vectors: step_i, the running sum S_i of step * A (block scan), the
-    // chunk's range of S and the split decay factors
     const float dt_raw = dt_next;
     dt_next = (t0 + Q + i < L) ? __bfloat162float(p.dt[((int64_t)b * L + t0 + Q + i) * p.H + h]) : 0.f;
-    float step = 0.f;
-    if (valid) {
+    step = 0.f;
+    if (t0 + i < L) {
       const float v = dt_raw + biash;
       step = p.softplus ? (v > 20.f ? v : log1pf(expf(v))) : v;
     }
@@ -378,7 +377,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     if (lane == 31) red[warp] = incl;
     __syncthreads();
     for (int w = 0; w < warp; ++w) incl += red[w];
-    const float Si = incl;
+    Si = incl;
     float mn = Si, mx = Si;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -394,12 +393,64 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     __syncthreads();
     mn = fminf(fminf(red[4], red[5]), fminf(red[6], red[7]));
     mx = fmaxf(fmaxf(red[8], red[9]), fmaxf(red[10], red[11]));
-    const float Slast = Sv[Q - 1];
+    Slast = Sv[Q - 1];
     // both factors within e^(+-80) (inside fp32) when the range of S is at most 160
-    const bool split = (mx - mn) <= 160.f;
+    split = (mx - mn) <= 160.f;
     const float Sref = 0.5f * (mn + mx);
-    const float ai = ex2f((Si - Sref) * kLog2e);
+    ai = ex2f((Si - Sref) * kLog2e);
     bv[i] = ex2f((Sref - Si) * kLog2e) * step;
+  };
+  // ---- the state entering a chunk (sum of its two accumulators): its bf16 copy (hi, lo)
+  // for C h_prev, then h <- exp(S_last) h into the first accumulator, zeros into the
+  // second.  Needs no input of the chunk, so it runs while the chunk's copies land.
+  auto state_copy = [&]() {
+    const float dl = ex2f(Slast * kLog2e);
+#pragma unroll 1
+    for (int nb = 0; nb < NP / 128; ++nb) {
+      const int n = nb * 128 + i;
+#pragma unroll 1
+      for (int c0 = 0; c0 < PB; c0 += 32) {
+        const uint32_t ta = lane_t + Sm::T_H + nb * 2 * PB + c0;
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nw(ta, ra);
+        tmem_ld32_nw(ta + PB, rb);
+        tmem_wait_ld(ra);
+        tmem_wait_ld(rb);
+        float v[32], zero[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+          zero[j] = 0.f;
+        }
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(v[cb * 8 + 2 * e], v[cb * 8 + 2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = cm(n, (c0 >> 3) + cb, NP);
+          *reinterpret_cast<uint4*>(smem + Sm::H_OFF + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(smem + Sm::H_OFF + NP * PB * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= dl;
+        tmem_st32(ta, v);
+        tmem_st32(ta + PB, zero);
+      }
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  };
+
+  // chunk 0's vectors and state copy
+  scan(0);
+  state_copy();
+
+  uint32_t cur = 0;  // phase parity of the chunk in hand
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const uint32_t par = c & 1;
+    cur = par;
+    const int64_t t0 = (int64_t)c * Q;
+    const bool valid = t0 + i < L;
 
     // ---- the chunk's inputs; G = C B^T (every wait is decided by all threads together,
     // so that they leave the loop at the same point)
@@ -440,44 +491,6 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
         *reinterpret_cast<uint4*>(smem + Sm::W_OFF + Q * PB * 2 + cm(i, cb, Q)) =
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-    }
-    // ---- the state (sum of its two accumulators): its bf16 copy (hi, lo) for C h_prev,
-    // then h <- exp(S_last) h into the first accumulator, zeros into the second
-    {
-      const float dl = ex2f(Slast * kLog2e);
-#pragma unroll 1
-      for (int nb = 0; nb < NP / 128; ++nb) {
-        const int n = nb * 128 + i;
-#pragma unroll 1
-        for (int c0 = 0; c0 < PB; c0 += 32) {
-          const uint32_t ta = lane_t + Sm::T_H + nb * 2 * PB + c0;
-          uint32_t ra[32], rb[32];
-          tmem_ld32_nw(ta, ra);
-          tmem_ld32_nw(ta + PB, rb);
-          tmem_wait_ld(ra);
-          tmem_wait_ld(rb);
-          float v[32], zero[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
-            zero[j] = 0.f;
-          }
-#pragma unroll
-          for (int cb = 0; cb < 4; ++cb) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) split2(v[cb * 8 + 2 * e], v[cb * 8 + 2 * e + 1], hi[e], lo[e]);
-            const uint32_t off = cm(n, (c0 >> 3) + cb, NP);
-            *reinterpret_cast<uint4*>(smem + Sm::H_OFF + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(smem + Sm::H_OFF + NP * PB * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= dl;
-          tmem_st32(ta, v);
-          tmem_st32(ta + PB, zero);
-        }
-      }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
     // ---- Yo = C h_prev (hi + lo); h += B^T Xw (hi + lo)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -566,16 +579,19 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     if (!__syncthreads_and(mbar_wait(bar_y, par))) { ok = false; break; }
     issued &= ~4;
     tc_fence_after();
-    // the tiles are consumed: fetch the next chunk's inputs while the outputs are formed
+    // the tiles are consumed: fetch the next chunk's inputs, and while they land form
+    // the next chunk's per-step vectors and state copy, then this chunk's outputs
+    const float ei = ex2f(Si * kLog2e);
     if (c + 1 < nch) {
       if (tid == 0) load_chunk(c + 1);
       in_flight = true;
+      scan(c + 1);
+      state_copy();
     }
 
     // ---- y = Yd + exp(S_i) Yo + D x; out = y silu(z).  The tensor-memory loads are
     // warp-wide (.sync.aligned): every lane takes them, only valid rows store.
     {
-      const float ei = ex2f(Si * kLog2e);
 #pragma unroll
       for (int c0 = 0; c0 < PB; c0 += 32) {
         float yd[32], yo[32];
