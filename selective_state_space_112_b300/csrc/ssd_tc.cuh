@@ -15,8 +15,9 @@
 //   y_i      = Yd_i + exp(S_i) Yo_i + D x_i;   out = y silu(z)
 //   h_next   = exp(S_last) h_prev + B^T Xw,   Xw_j = exp(S_last - S_j) step_j x_j
 // The four products are tcgen05.mma (kind::f16: bf16 operands, fp32 accumulators in
-// TMEM), issued by one thread and completed on mbarriers.  Operands sit in shared
-// memory in the no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix,
+// TMEM), each accumulator chain issued by one thread (C h_prev and B^T Xw, and the two
+// parts of M X, by two threads side by side) and completed on mbarriers.  Operands sit
+// in shared memory in the no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix,
 // blocks of 8 columns stored one after another): C, B and x arrive that way by TMA
 // tensor copies (one 5-D box per tensor and chunk, whose dimensions -- 8 columns, Q
 // rows, the blocks of 8 columns -- lay the tile out block by block); M, Xw and the
@@ -281,9 +282,10 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
 
   // zero the tiles once (the rows of B past N feed state rows that are never read)
   for (int i = tid; i < Sm::V_OFF / 16; i += NTHR) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
+  if (tid == 0) {  // C h_prev and B^T Xw, and the two parts of M X, are issued by two threads
+    const uint32_t cnt[4] = {1, 1, 2, 2};
     for (int i = 0; i < 4; ++i)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[i])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&bars[i])), "r"(cnt[i]) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -496,17 +498,16 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0) {  // C h_prev (K = n)
       tc_fence_after();
-      // the two chains interleaved: C h_prev (K = n) and, per 128 state rows, B^T Xw (K = j)
-      const int kmax = kN > Q / 16 ? kN : Q / 16;
-      for (int k = 0; k < kmax; ++k) {
-        if (k < kN) mma(tmem + Sm::T_YO, dC + off16(k * 2 * Q * 16), dH + off16(k * 256), ID_O, k > 0);
-        if (k < Q / 16)
-          for (int nb = 0; nb < NP / 128; ++nb)
-            mma(tmem + Sm::T_H + nb * 2 * PB, dBt + off16(nb * 16 * Q * 16 + k * 256), dW + off16(k * 256), ID_S,
-                true);
-      }
+      for (int k = 0; k < kN; ++k) mma(tmem + Sm::T_YO, dC + off16(k * 2 * Q * 16), dH + off16(k * 256), ID_O, k > 0);
+      mma_commit(bar_s);
+    } else if (tid == 32) {  // per 128 state rows, B^T Xw (K = j)
+      tc_fence_after();
+      for (int k = 0; k < Q / 16; ++k)
+        for (int nb = 0; nb < NP / 128; ++nb)
+          mma(tmem + Sm::T_H + nb * 2 * PB, dBt + off16(nb * 16 * Q * 16 + k * 256), dW + off16(k * 256), ID_S,
+              true);
       mma_commit(bar_s);
     }
     issued |= 2;
@@ -567,12 +568,12 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 || tid == 32) {  // M_hi X and M_lo X, two chains in the columns of G
       tc_fence_after();
-      for (int k = 0; k < Q / 16; ++k) {  // M_hi X and M_lo X, two chains in the columns of G
-        mma(tmem + Sm::T_G, dM + off16(k * 2 * Q * 16), dX + off16(k * 256), ID_Y, k > 0);
-        mma(tmem + Sm::T_G + PB, dM + off16(Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 256), ID_Y, k > 0);
-      }
+      const uint32_t part = tid >> 5;
+      for (int k = 0; k < Q / 16; ++k)
+        mma(tmem + Sm::T_G + part * PB, dM + off16(part * Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 256), ID_Y,
+            k > 0);
       mma_commit(bar_y);
     }
     issued |= 4;
