@@ -89,6 +89,18 @@ def test_long_bf16_sampled():
     sampled_check(config("long_bf16"), 48, 4)
 
 
+def test_long_bf16_sampled_one_launch():
+    """The same layer with the one-launch (decoupled lookback) carry: 22 chunks, each
+    folding all of its predecessors' published aggregates; sampled channels against
+    the oracle and the whole output bitwise equal to a second run."""
+    import selective_state_space_112_b300 as ssm
+    ssm.ssm_set_option("one_launch", 1)
+    w = config("long_bf16")
+    g_out, g_fs = sampled_check(w, 32, 5)
+    g_out2, g_fs2 = run_gpu(w)
+    assert np.array_equal(g_out, g_out2) and np.array_equal(g_fs, g_fs2)
+
+
 def test_step_bf16_full():
     """Recurrent step: L = 1 with a stored state, every output and state checked."""
     full_check(config("step_bf16"), "step_bf16")
