@@ -267,6 +267,20 @@ uint64_t ssm_kernel_launches(void);
  *                   for that tile run out (every wait of a kernel is bounded by 2 s);
  *                   the kernels return and ssm_check_status reports SSM_ERR_TIMEOUT.
  *                   Leave it 0 otherwise.
+ *   "one_launch"    0 (default): the cross-chunk carry is an aggregate pass (each
+ *                   chunk's end state from zero and its step sum) and a fold in the
+ *                   output pass, two launches; 1: one launch with decoupled lookback
+ *                   (pages "State-space models", The parallel scan; "Structured State
+ *                   Space Models and Mamba", Hardware-Aware Parallel Associative Scan):
+ *                   chunks take tickets from a counter, publish their aggregates with
+ *                   flags and fold their predecessors' aggregates in a fixed order, so
+ *                   results stay bitwise repeatable.  Flag waits are bounded (2 s,
+ *                   SSM_ERR_TIMEOUT).
+ *   "hold_chunk"    failure injection for tests (0 = off, with "one_launch" 1): with
+ *                   value k, chunk k - 1 never publishes its aggregate, so the flag
+ *                   waits of its successors run out.  Leave it 0 otherwise.
+ *   "ssd_legacy"    0 (default): ssm_ssd_fwd runs the tcgen05 kernel; 1: the earlier
+ *                   mma.sync kernel (kept for comparison).
  * Returns SSM_ERR_DIMS for an unknown name or a negative value.
  */
 int ssm_set_option(const char* name, int64_t value);
