@@ -22,10 +22,12 @@
 // tensor copies (one 5-D box per tensor and chunk, whose dimensions -- 8 columns, Q
 // rows, the blocks of 8 columns -- lay the tile out block by block); M, Xw and the
 // state copy are written there by the threads.  Thread i owns TMEM lane i (row i of
-// every accumulator) for the element-wise work.  A value held as a pair of bf16 parts
-// enters a product as one operand twice as wide (parts side by side), so that one
-// instruction forms both partial products into adjacent accumulator columns; the
-// carried state is held as two accumulators (the sum so far, this chunk's low parts).
+// every accumulator) for the element-wise work.  The state copy and Xw, held as pairs
+// of bf16 parts, enter their products as one operand twice as wide (the parts side by
+// side), so that one instruction forms both partial products into adjacent accumulator
+// columns; the carried state is held as two accumulators (the sum so far, this chunk's
+// low parts).  The two parts of M enter as two products (M_hi X, M_lo X), summed when
+// the outputs are formed.
 //
 // Order inside a chunk: G is issued as soon as the inputs land; while it runs the
 // threads form Xw, then C h_prev and B^T Xw are issued; M is formed from G once those
@@ -36,11 +38,12 @@
 //   exp(S_i - S_j) = exp(S_i - S_ref) exp(S_ref - S_j),  S_ref = the midpoint of the
 // chunk's range of S, so that M costs two multiplies per element; a chunk whose range
 // of S is too wide for both factors to stay inside fp32 takes one exponential per
-// element instead.  Rows above the diagonal block of a warp are zero and not formed.
+// element instead.  The column blocks right of a warp's diagonal block are zero and
+// not formed.
 //
 // Precision: the operands formed in fp32 enter as a pair of bf16 values (value and
-// remainder, about 16 significant bits): M (one bf16 rounding of it would cost up to
-// about 1e-2 of floored error on Gaussian inputs), Xw and the state copy (the state
+// remainder, about 16 significant bits): M (one bf16 rounding of it alone reached
+// 1.7e-2 of floored error on a Gaussian layer), Xw and the state copy (the state
 // accumulates over the whole sequence).  Step sizes, decays and the state stay in
 // fp32.  Every wait is bounded (2 s); a wait that runs out sets the status word and
 // the CTA waits (bounded) for its products in flight, frees its tensor memory and
