@@ -564,11 +564,12 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t strea
   std::memset(&p, 0, sizeof p);
   p.x = prm.x; p.dt = prm.dt; p.z = prm.z; p.A = prm.A; p.D = prm.D; p.dt_bias = prm.dt_bias;
   p.out = prm.out; p.state = prm.state; p.L = prm.L; p.H = prm.H; p.G = prm.G; p.hpg = prm.hpg;
-  p.N = N; p.softplus = prm.softplus; p.state_in = prm.state_in;
+  p.N = N; p.softplus = prm.softplus; p.state_in = prm.state_in; p.batch = (int)batch;
   p.status = ssm_internal::status_word();
   if (!p.status) return SSM_ERR_CUDA;
-  ssd::ssd_tc_kernel<NP, PB><<<dim3((unsigned)prm.H * (ssd::P / PB), (unsigned)batch), ssd::NTHR, Sm::BYTES,
-                               stream>>>(maps, p);
+  const int64_t ctas = (int64_t)prm.H * (ssd::P / PB) * batch;
+  if (ctas > INT32_MAX) return SSM_ERR_DIMS;
+  ssd::ssd_tc_kernel<NP, PB><<<dim3((unsigned)ctas), ssd::NTHR, Sm::BYTES, stream>>>(maps, p);
   ssm_internal::count_launch();
   return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

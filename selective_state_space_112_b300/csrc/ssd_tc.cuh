@@ -80,7 +80,7 @@ struct Params {
   float* state;       // (batch, H, P, N) or null
   int* status;
   int64_t L;
-  int H, G, hpg, N;
+  int batch, H, G, hpg, N;
   int softplus, state_in;
 };
 
@@ -267,8 +267,11 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x / (P / PB), pc = (blockIdx.x % (P / PB)) * PB;  // head, first channel
-  const int b = blockIdx.y, g = h / p.hpg;
+  // batch row fastest: the CTAs resident at one time spread over every batch row, so
+  // that they do not all read the same C, B tile from L2 at once
+  const int b = (int)(blockIdx.x % (unsigned)p.batch), hb = (int)(blockIdx.x / (unsigned)p.batch);
+  const int h = hb / (P / PB), pc = (hb % (P / PB)) * PB;  // head, first channel
+  const int g = h / p.hpg;
   const int64_t L = p.L;
   const int nch = (int)((L + Q - 1) / Q);
   const int N = p.N, kN = p.N / 16;  // K steps over the state dimension
