@@ -523,21 +523,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A (batch, L, mid, inner) bf16 tensor seen as 5-D: (8 values, L rows, inner / 8
-// blocks of 8 values, mid, batch).  A box of (8, Q, blocks, 1, 1) lands in shared memory
-// block by block, each block Q rows of 16 bytes: the no-swizzle core-matrix layout of
-// the tensor-core operands.
+// A (batch, L, mid, inner) bf16 tensor seen as 5-D: (w values, L rows, inner / w blocks
+// of w values, mid, batch).  A box of (w, Q, blocks, 1, 1) lands in shared memory block
+// by block, each block Q rows of w values swizzled as the tensor cores read them
+// (w = 64 with the 128-byte swizzle, w = 32 with the 64-byte swizzle).
 bool encode_tile(CUtensorMap* m, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch,
-                 int blocks) {
+                 int w, int blocks, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[5] = {8, (cuuint64_t)L, (cuuint64_t)(inner / 8), (cuuint64_t)mid, (cuuint64_t)batch};
-  const cuuint64_t strides[4] = {(cuuint64_t)(inner * mid * 2), 16, (cuuint64_t)(inner * 2),
+  if (!fn || inner % w) return false;
+  const cuuint64_t dims[5] = {(cuuint64_t)w, (cuuint64_t)L, (cuuint64_t)(inner / w), (cuuint64_t)mid,
+                              (cuuint64_t)batch};
+  const cuuint64_t strides[4] = {(cuuint64_t)(inner * mid * 2), (cuuint64_t)(w * 2), (cuuint64_t)(inner * 2),
                                  (cuuint64_t)(inner * mid * L * 2)};
-  const cuuint32_t box[5] = {8, (cuuint32_t)ssd::Q, (cuuint32_t)blocks, 1, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)w, (cuuint32_t)ssd::Q, (cuuint32_t)blocks, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -556,9 +557,9 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t strea
   }
   ssd::Maps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (!encode_tile(&maps.x, prm.x, P, prm.H, prm.L, batch, PB / 8) ||
-      !encode_tile(&maps.B, prm.B, N, prm.G, prm.L, batch, N / 8) ||
-      !encode_tile(&maps.C, prm.C, N, prm.G, prm.L, batch, N / 8))
+  if (!encode_tile(&maps.x, prm.x, P, prm.H, prm.L, batch, PB, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_tile(&maps.B, prm.B, N, prm.G, prm.L, batch, 64, N / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tile(&maps.C, prm.C, N, prm.G, prm.L, batch, 64, N / 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return SSM_ERR_CUDA;
   ssd::Params p;
   std::memset(&p, 0, sizeof p);

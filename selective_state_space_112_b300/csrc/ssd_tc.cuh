@@ -61,11 +61,12 @@ constexpr int P = 64;       // channels per head
 constexpr int NTHR = 128;   // threads per CTA: one per TMEM lane
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// 5-D tensor maps (8 columns, L rows, blocks of 8 columns, head or group, batch row):
-// one box of (8, Q, blocks, 1, 1) is a chunk's tile in the core-matrix layout.
+// 5-D tensor maps (w values, L rows, blocks of w values, head or group, batch row): one
+// box of (w, Q, blocks, 1, 1) is a chunk's tile, block by block, each block Q swizzled
+// rows of w values (C, B: w = 64, 128-byte swizzle; x: w = PB = 32, 64-byte swizzle).
 struct Maps {
-  CUtensorMap x;   // box (8, Q, PB / 8, 1, 1)
-  CUtensorMap B;   // box (8, Q, N / 8, 1, 1)
+  CUtensorMap x;   // box (32, Q, 1, 1, 1)
+  CUtensorMap B;   // box (64, Q, N / 64, 1, 1)
   CUtensorMap C;
 };
 
@@ -106,6 +107,8 @@ struct Smem {
   static_assert(TUSED <= 512, "tensor memory columns");
   static_assert(2 * Q * Q * 2 <= X_OFF, "M (hi, lo) fits in the space of C and B");
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
+  static_assert(PB == 32, "x arrives as 64-byte swizzled rows of 32 channels");
+  static_assert(B_OFF % 1024 == 0 && X_OFF % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -142,13 +145,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t par) {
   return false;
 }
 
-// Shared-memory matrix descriptor, no swizzle: start address, leading-dimension byte
-// offset (between core matrices along K), stride-dimension byte offset (between core
-// matrices along M or N), the fixed version bits.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor: start address, leading-dimension byte offset,
+// stride-dimension byte offset, the fixed version bits and the layout (0: no swizzle,
+// core matrices of 8 rows x 16 bytes; kSw128 / kSw64: rows of 128 / 64 bytes with their
+// 16-byte pieces permuted within groups of 8 rows, as TMA writes them).  No swizzle:
+// LBO between core matrices along K, SBO between core matrices along M or N.  Swizzled
+// K-major: SBO between groups of 8 rows (LBO unused); swizzled MN-major: LBO between
+// blocks of 64 (128 B) or 32 (64 B) M/N values, SBO between groups of 8 K rows.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
   return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
+// layout field of a shared-memory descriptor
+constexpr uint32_t kSw128 = 2, kSw64 = 4;
+constexpr int kAtom = Q * 128;  // one 128-byte-swizzled block: Q rows of 64 bf16 values
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N, K-major (0) or
 // MN-major (1) A and B.
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     const int t0 = c * Q;
     tma_load_5d(s_base + Sm::C_OFF, &maps.C, 0, t0, 0, g, b, bar_in);
     tma_load_5d(s_base + Sm::B_OFF, &maps.B, 0, t0, 0, g, b, bar_in);
-    tma_load_5d(s_base + Sm::X_OFF, &maps.x, 0, t0, pc / 8, h, b, bar_in);
+    tma_load_5d(s_base + Sm::X_OFF, &maps.x, 0, t0, pc / PB, h, b, bar_in);
   };
   if (tid == 0) load_chunk(0);
   bool in_flight = true;  // a tensor copy into the tiles has been issued and not waited for
@@ -349,13 +359,17 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   constexpr uint32_t ID_O = idesc(Q, 2 * PB, 0, 1);     // C (K-major) x [h_hi | h_lo] (MN-major)
   constexpr uint32_t ID_S = idesc(128, 2 * PB, 1, 1);   // B^T (MN-major) x [Xw_hi | Xw_lo] (MN-major)
   // operand descriptors at offset 0; a K step adds its byte offset / 16
-  const uint64_t dC = sdesc(s_base + Sm::C_OFF, Q * 16, 128);    // K-major, K = n
-  const uint64_t dB = sdesc(s_base + Sm::B_OFF, Q * 16, 128);    // K-major, K = n
-  const uint64_t dBt = sdesc(s_base + Sm::B_OFF, 128, Q * 16);   // MN-major: M = n, K = j
-  const uint64_t dH = sdesc(s_base + Sm::H_OFF, 128, NP * 16);   // MN-major: N = channel, K = n
-  const uint64_t dW = sdesc(s_base + Sm::W_OFF, 128, Q * 16);    // MN-major: N = channel, K = j
-  const uint64_t dM = sdesc(s_base + Sm::M_OFF, Q * 16, 128);    // K-major, K = j
-  const uint64_t dX = sdesc(s_base + Sm::X_OFF, 128, Q * 16);    // MN-major: N = channel, K = j
+  // C, B, x arrive 128- (C, B) and 64-byte (x) swizzled; M, Xw, the state copy are
+  // written by the threads without swizzle
+  const uint64_t dC = sdesc(s_base + Sm::C_OFF, 16, 1024, kSw128);      // K-major, K = n
+  const uint64_t dB = sdesc(s_base + Sm::B_OFF, 16, 1024, kSw128);      // K-major, K = n
+  const uint64_t dBt = sdesc(s_base + Sm::B_OFF, kAtom, 1024, kSw128);  // MN-major: M = n, K = j
+  const uint64_t dX = sdesc(s_base + Sm::X_OFF, 4096, 512, kSw64);      // MN-major: N = channel, K = j
+  const uint64_t dH = sdesc(s_base + Sm::H_OFF, 128, NP * 16);          // MN-major: N = channel, K = n
+  const uint64_t dW = sdesc(s_base + Sm::W_OFF, 128, Q * 16);           // MN-major: N = channel, K = j
+  const uint64_t dM = sdesc(s_base + Sm::M_OFF, Q * 16, 128);           // K-major, K = j
+  // a K step (16 values) of the swizzled K-major tiles: 32 bytes inside a block of 64
+  auto kmaj = [](int k) { return (uint32_t)((k >> 2) * kAtom + (k & 3) * 32); };
   auto off16 = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
 
   // the raw step of this thread's row, one chunk ahead
@@ -467,7 +481,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     if (tid == 0) {
       tc_fence_after();
       for (int k = 0; k < kN; ++k)
-        mma(tmem + Sm::T_G, dC + off16(k * 2 * Q * 16), dB + off16(k * 2 * Q * 16), ID_G, k > 0);
+        mma(tmem + Sm::T_G, dC + off16(kmaj(k)), dB + off16(kmaj(k)), ID_G, k > 0);
       mma_commit(bar_g);
     }
     issued |= 1;
@@ -486,7 +500,8 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       const float wj = ex2f((Slast - Si) * kLog2e) * step;
 #pragma unroll
       for (int cb = 0; cb < PB / 8; ++cb) {
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + Sm::X_OFF + cm(i, cb, Q));
+        // row i of x: 64 bytes, its 16-byte pieces permuted by bits 1-2 of the row
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + Sm::X_OFF + i * 64 + ((cb ^ ((i >> 1) & 3)) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -506,13 +521,13 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     __syncthreads();
     if (tid == 0) {  // C h_prev (K = n)
       tc_fence_after();
-      for (int k = 0; k < kN; ++k) mma(tmem + Sm::T_YO, dC + off16(k * 2 * Q * 16), dH + off16(k * 256), ID_O, k > 0);
+      for (int k = 0; k < kN; ++k) mma(tmem + Sm::T_YO, dC + off16(kmaj(k)), dH + off16(k * 256), ID_O, k > 0);
       mma_commit(bar_s);
     } else if (tid == 32) {  // per 128 state rows, B^T Xw (K = j)
       tc_fence_after();
       for (int k = 0; k < Q / 16; ++k)
         for (int nb = 0; nb < NP / 128; ++nb)
-          mma(tmem + Sm::T_H + nb * 2 * PB, dBt + off16(nb * 16 * Q * 16 + k * 256), dW + off16(k * 256), ID_S,
+          mma(tmem + Sm::T_H + nb * 2 * PB, dBt + off16(nb * 2 * kAtom + k * 16 * 128), dW + off16(k * 256), ID_S,
               true);
       mma_commit(bar_s);
     }
@@ -578,7 +593,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       tc_fence_after();
       const uint32_t part = tid >> 5;
       for (int k = 0; k < Q / 16; ++k)
-        mma(tmem + Sm::T_G + part * PB, dM + off16(part * Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 256), ID_Y,
+        mma(tmem + Sm::T_G + part * PB, dM + off16(part * Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 16 * 64), ID_Y,
             k > 0);
       mma_commit(bar_y);
     }
