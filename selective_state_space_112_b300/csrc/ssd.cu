@@ -542,15 +542,15 @@ bool encode_tile(CUtensorMap* m, const void* base, int64_t inner, int64_t mid, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NP, int PB>
-int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t stream) {
+template <int NP, int PB, int N>
+int launch_ssd_tc(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
   using Sm = ssd::Smem<NP, PB>;
   static std::atomic<uint64_t> ready{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(ready.load() & bit)) {
-    if (cudaFuncSetAttribute(ssd::ssd_tc_kernel<NP, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(ssd::ssd_tc_kernel<NP, PB, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Sm::BYTES) != cudaSuccess)
       return SSM_ERR_CUDA;
     ready.fetch_or(bit);
@@ -570,7 +570,7 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, int N, cudaStream_t strea
   if (!p.status) return SSM_ERR_CUDA;
   const int64_t ctas = (int64_t)prm.H * (ssd::P / PB) * batch;
   if (ctas > INT32_MAX) return SSM_ERR_DIMS;
-  ssd::ssd_tc_kernel<NP, PB><<<dim3((unsigned)ctas), ssd::NTHR, Sm::BYTES, stream>>>(maps, p);
+  ssd::ssd_tc_kernel<NP, PB, N><<<dim3((unsigned)ctas), ssd::NTHR, Sm::BYTES, stream>>>(maps, p);
   ssm_internal::count_launch();
   return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -641,9 +641,9 @@ extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const 
   prm.state_in = d.state_in;
   if (!g_ssd_legacy.load()) {
     switch (d.dstate) {
-      case 64: return launch_ssd_tc<128, 32>(prm, d.batch, 64, stream);  // state rows padded to 128
-      case 128: return launch_ssd_tc<128, 32>(prm, d.batch, 128, stream);
-      default: return launch_ssd_tc<256, 32>(prm, d.batch, 256, stream);
+      case 64: return launch_ssd_tc<128, 32, 64>(prm, d.batch, stream);  // state rows padded to 128
+      case 128: return launch_ssd_tc<128, 32, 128>(prm, d.batch, stream);
+      default: return launch_ssd_tc<256, 32, 256>(prm, d.batch, stream);
     }
   }
   switch (d.dstate) {

@@ -270,9 +270,11 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // R rows whose column blocks are stored one after another (block cb at cb * R * 16).
 __device__ __forceinline__ uint32_t cm(int r, int cb, int R) { return (uint32_t)(cb * R + r) * 16u; }
 
-template <int NP, int PB>
+// NN = N (a compile-time state size: the product loops unroll with constant descriptors)
+template <int NP, int PB, int NN>
 __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::TCOLS <= 256) ? 2 : 1)
     ssd_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  static_assert(NN % 64 == 0 && NN <= NP, "state size: a multiple of 64, at most the padded rows");
   using Sm = Smem<NP, PB>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   const int g = h / p.hpg;
   const int64_t L = p.L;
   const int nch = (int)((L + Q - 1) / Q);
-  const int N = p.N, kN = p.N / 16;  // K steps over the state dimension
+  constexpr int N = NN, kN = NN / 16;  // K steps over the state dimension
   const float Ah = p.A[h], Dh = p.D ? p.D[h] : 0.f, biash = p.dt_bias ? p.dt_bias[h] : 0.f;
   float* Sv = reinterpret_cast<float*>(smem + Sm::V_OFF);  // S_i of the chunk
   float* stepv = Sv + Q;                                  // step_i
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     in_flight = false;
     if (tid == 0) {
       tc_fence_after();
+#pragma unroll
       for (int k = 0; k < kN; ++k)
         mma(tmem + Sm::T_G, dC + off16(kmaj(k)), dB + off16(kmaj(k)), ID_G, k > 0);
       mma_commit(bar_g);
@@ -521,6 +524,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     __syncthreads();
     if (tid == 0) {  // C h_prev (K = n)
       tc_fence_after();
+#pragma unroll
       for (int k = 0; k < kN; ++k) mma(tmem + Sm::T_YO, dC + off16(kmaj(k)), dH + off16(k * 256), ID_O, k > 0);
       mma_commit(bar_s);
     } else if (tid == 32) {  // per 128 state rows, B^T Xw (K = j)
