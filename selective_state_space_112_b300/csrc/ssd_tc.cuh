@@ -16,30 +16,31 @@
 //   h_next   = exp(S_last) h_prev + B^T Xw,   Xw_j = exp(S_last - S_j) step_j x_j
 // The four products are tcgen05.mma (kind::f16: bf16 operands, fp32 accumulators in
 // TMEM), each accumulator chain issued by one thread (C h_prev and B^T Xw, and the two
-// parts of M X, by two threads side by side) and completed on mbarriers.  Operands sit
-// in shared memory in the no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix,
-// blocks of 8 columns stored one after another): C, B and x arrive that way by TMA
-// tensor copies (one 5-D box per tensor and chunk, whose dimensions -- 8 columns, Q
-// rows, the blocks of 8 columns -- lay the tile out block by block); M, Xw and the
-// state copy are written there by the threads.  Thread i owns TMEM lane i (row i of
-// every accumulator) for the element-wise work.  The state copy and Xw, held as pairs
-// of bf16 parts, enter their products as one operand twice as wide (the parts side by
-// side), so that one instruction forms both partial products into adjacent accumulator
-// columns; the carried state is held as two accumulators (the sum so far, this chunk's
-// low parts).  The two parts of M enter as two products (M_hi X, M_lo X), summed when
-// the outputs are formed.
+// parts of M X, by two threads side by side) and completed on mbarriers.  C, B and x
+// arrive by one TMA tensor copy each per chunk, as rows of 128 (C, B) and 64 (x) bytes
+// with the hardware swizzle, and enter the products through swizzled shared-memory
+// descriptors; Xw and the state copy are written by the threads in the no-swizzle
+// core-matrix layout (8 rows x 16 bytes per core matrix).  M never leaves tensor memory:
+// each thread reads its row of G, forms its row of M and writes it back over G as the A
+// operand of M X.  Thread i owns TMEM lane i (row i of every accumulator) for the
+// element-wise work.  The state copy and Xw, held as pairs of bf16 parts, enter their
+// products as one operand twice as wide (the parts side by side), so that one
+// instruction forms both partial products into adjacent accumulator columns; the carried
+// state is held as two accumulators (the sum so far, this chunk's low parts).  The two
+// parts of M enter as two products (M_hi X onto exp(S_i) C h_prev, M_lo X beside it),
+// summed when the outputs are formed.
 //
 // Order inside a chunk: G is issued as soon as the inputs land; while it runs the
-// threads form Xw, then C h_prev and B^T Xw are issued; M is formed from G once those
-// products are done, into the space of C and B (no longer read), and M X is issued
-// last.  Then the next chunk's copies are issued, and while they land the threads form
-// the next chunk's per-step vectors and state copy (neither needs its inputs) and this
-// chunk's outputs.  The decay factor of M is split as
+// threads form Xw, then C h_prev and B^T Xw are issued; M is formed once G is done, the
+// scaled C h_prev written as the start of M X once those two are done, and M X is
+// issued last.  Then the next chunk's copies are issued, and while they land the threads
+// form the next chunk's per-step vectors and state copy (neither needs its inputs) and
+// this chunk's outputs.  The decay factor of M is split as
 //   exp(S_i - S_j) = exp(S_i - S_ref) exp(S_ref - S_j),  S_ref = the midpoint of the
 // chunk's range of S, so that M costs two multiplies per element; a chunk whose range
 // of S is too wide for both factors to stay inside fp32 takes one exponential per
 // element instead.  The column blocks right of a warp's diagonal block are zero and
-// not formed.
+// written as zeros, not formed.
 //
 // Precision: the operands formed in fp32 enter as a pair of bf16 values (value and
 // remainder, about 16 significant bits): M (one bf16 rounding of it alone reached
@@ -86,26 +87,24 @@ struct Params {
 };
 
 // Shared-memory plan of one CTA: NP = N padded to a multiple of 128 (the state rows
-// of one product), PB channels.  M (hi, lo) reuses the space of C and B.
+// of one product), PB channels.
 template <int NP, int PB>
 struct Smem {
   static constexpr int C_OFF = 0;                        // C tile  [Q x NP] bf16
   static constexpr int B_OFF = C_OFF + Q * NP * 2;       // B tile  [Q x NP]
-  static constexpr int M_OFF = 0;                        // M hi, lo [Q x Q] each
   static constexpr int X_OFF = B_OFF + Q * NP * 2;       // x tile  [Q x PB]
   static constexpr int W_OFF = X_OFF + Q * PB * 2;       // Xw hi, lo [Q x PB] each
   static constexpr int H_OFF = W_OFF + 2 * Q * PB * 2;   // state hi, lo [NP x PB] each
   static constexpr int V_OFF = H_OFF + 2 * NP * PB * 2;  // S, step, b (Q floats each), reductions
   static constexpr int BAR_OFF = V_OFF + 3 * Q * 4 + 64;
   static constexpr int BYTES = BAR_OFF + 64;
-  // TMEM columns: G (then M_hi X and M_lo X in its first 2 PB columns), C h_hi | C h_lo,
-  // and per 128 state rows the state's two accumulators (sum so far | low parts)
+  // TMEM columns: G, then M (hi, lo: two bf16 per column) in its place; C h_hi | C h_lo,
+  // then the two M X accumulators in their place; per 128 state rows the state's two
+  // accumulators (sum so far | low parts)
   static constexpr int T_G = 0, T_YO = Q, T_H = Q + 2 * PB;
   static constexpr int TUSED = T_H + (NP / 128) * 2 * PB;
-  static_assert(2 * PB <= Q, "the products M X fit in the columns of G");
   static constexpr int TCOLS = TUSED <= 256 ? 256 : 512;
   static_assert(TUSED <= 512, "tensor memory columns");
-  static_assert(2 * Q * Q * 2 <= X_OFF, "M (hi, lo) fits in the space of C and B");
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
   static_assert(PB == 32, "x arrives as 64-byte swizzled rows of 32 channels");
   static_assert(B_OFF % 1024 == 0 && X_OFF % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
@@ -175,6 +174,16 @@ __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t da, uint64_t db, u
       : "memory");
 }
 
+// The same with A (M x 16, K-major) in tensor memory: row m in lane m, two bf16 values
+// of K per column (the lower K in the low half), the 8 columns of a K step from tmem_a.
+__device__ __forceinline__ void mma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -219,22 +228,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+  tmem_st32u(taddr, r);
 }
 
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
@@ -357,11 +366,11 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   bool in_flight = true;  // a tensor copy into the tiles has been issued and not waited for
 
   constexpr uint32_t ID_G = idesc(Q, Q, 0, 0);          // C (K-major) x B^T (K-major)
-  constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);         // M (K-major) x X (MN-major)
+  constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);         // M (TMEM) x X (MN-major)
   constexpr uint32_t ID_O = idesc(Q, 2 * PB, 0, 1);     // C (K-major) x [h_hi | h_lo] (MN-major)
   constexpr uint32_t ID_S = idesc(128, 2 * PB, 1, 1);   // B^T (MN-major) x [Xw_hi | Xw_lo] (MN-major)
   // operand descriptors at offset 0; a K step adds its byte offset / 16
-  // C, B, x arrive 128- (C, B) and 64-byte (x) swizzled; M, Xw, the state copy are
+  // C, B, x arrive 128- (C, B) and 64-byte (x) swizzled; Xw and the state copy are
   // written by the threads without swizzle
   const uint64_t dC = sdesc(s_base + Sm::C_OFF, 16, 1024, kSw128);      // K-major, K = n
   const uint64_t dB = sdesc(s_base + Sm::B_OFF, 16, 1024, kSw128);      // K-major, K = n
@@ -369,7 +378,6 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   const uint64_t dX = sdesc(s_base + Sm::X_OFF, 4096, 512, kSw64);      // MN-major: N = channel, K = j
   const uint64_t dH = sdesc(s_base + Sm::H_OFF, 128, NP * 16);          // MN-major: N = channel, K = n
   const uint64_t dW = sdesc(s_base + Sm::W_OFF, 128, Q * 16);           // MN-major: N = channel, K = j
-  const uint64_t dM = sdesc(s_base + Sm::M_OFF, Q * 16, 128);           // K-major, K = j
   // a K step (16 values) of the swizzled K-major tiles: 32 bytes inside a block of 64
   auto kmaj = [](int k) { return (uint32_t)((k >> 2) * kAtom + (k & 3) * 32); };
   auto off16 = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
@@ -537,15 +545,17 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     }
     issued |= 2;
 
-    // ---- M[i][j] = G[i][j] exp(S_i - S_j) step_j (j <= i), hi + lo, over the space of C
-    // and B once the products reading them are done
+    // ---- M[i][j] = G[i][j] exp(S_i - S_j) step_j (j <= i) as a pair of bf16 (hi, lo),
+    // written over G in tensor memory: per K step of 16 columns of M, 8 columns of packed
+    // hi values, then 8 of lo values (a column block of G becomes exactly the two K steps
+    // of M it holds, so each warp overwrites only what it has just read)
     if (!__syncthreads_and(mbar_wait(bar_g, par))) { ok = false; break; }
     issued &= ~1;
     tc_fence_after();
 #pragma unroll 1
     for (int J = 0; J < Q / 32; ++J) {
       const int j0 = J * 32;
-      uint32_t hi[16], lo[16];
+      uint32_t mv[32];  // [hi 0-7 | lo 0-7 | hi 8-15 | lo 8-15] of the block's 16 pairs
       if (J <= warp) {  // warp-uniform: blocks right of the diagonal block are zero
         float gv[32];
         tmem_ld32(lane_t + Sm::T_G + j0, gv);
@@ -568,37 +578,44 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
           for (int jj = 0; jj < 32; ++jj) m[jj] = (j0 + jj <= i) ? m[jj] : 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) split2(m[2 * e], m[2 * e + 1], hi[e], lo[e]);
+        for (int e = 0; e < 16; ++e)
+          split2(m[2 * e], m[2 * e + 1], mv[(e >> 3) * 16 + (e & 7)], mv[(e >> 3) * 16 + 8 + (e & 7)]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+        for (int e = 0; e < 32; ++e) mv[e] = 0u;
       }
-      if (J == 0) {
-        if (!__syncthreads_and(mbar_wait(bar_s, par))) ok = false;
-        tc_fence_after();
-      }
-      if (!ok) break;
+      tmem_st32u(lane_t + Sm::T_G + j0, mv);
+    }
+    // ---- the first M X accumulator starts from exp(S_i) C h_prev (C h_hi + C h_lo), in
+    // the place of C h_hi; the second starts from zero in the place of C h_lo
+    if (!__syncthreads_and(mbar_wait(bar_s, par))) { ok = false; break; }
+    issued &= ~2;
+    tc_fence_after();
+    {
+      const float ei = ex2f(Si * kLog2e);
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const uint32_t off = cm(i, J * 4 + cb, Q);
-        *reinterpret_cast<uint4*>(smem + Sm::M_OFF + off) =
-            make_uint4(hi[4 * cb], hi[4 * cb + 1], hi[4 * cb + 2], hi[4 * cb + 3]);
-        *reinterpret_cast<uint4*>(smem + Sm::M_OFF + Q * Q * 2 + off) =
-            make_uint4(lo[4 * cb], lo[4 * cb + 1], lo[4 * cb + 2], lo[4 * cb + 3]);
+      for (int c0 = 0; c0 < PB; c0 += 32) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nw(lane_t + Sm::T_YO + c0, ra);
+        tmem_ld32_nw(lane_t + Sm::T_YO + PB + c0, rb);
+        tmem_wait_ld(ra);
+        tmem_wait_ld(rb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ra[j] = __float_as_uint(ei * (__uint_as_float(ra[j]) + __uint_as_float(rb[j])));
+        tmem_st32u(lane_t + Sm::T_YO + c0, ra);
       }
     }
-    if (!ok) break;
-    issued &= ~2;
-    // ---- Yd = M X (hi + lo)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    // ---- Yd = M X: M_hi X onto exp(S) C h_prev, M_lo X beside it; A from tensor memory
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 || tid == 32) {  // M_hi X and M_lo X, two chains in the columns of G
+    if (tid == 0 || tid == 32) {
       tc_fence_after();
       const uint32_t part = tid >> 5;
+#pragma unroll
       for (int k = 0; k < Q / 16; ++k)
-        mma(tmem + Sm::T_G + part * PB, dM + off16(part * Q * Q * 2 + k * 2 * Q * 16), dX + off16(k * 16 * 64), ID_Y,
-            k > 0);
+        mma_ta(tmem + Sm::T_YO + part * PB, tmem + Sm::T_G + k * 16 + part * 8, dX + off16(k * 16 * 64), ID_Y,
+               part == 0 || k > 0);
       mma_commit(bar_y);
     }
     issued |= 4;
@@ -607,7 +624,6 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     tc_fence_after();
     // the tiles are consumed: fetch the next chunk's inputs, and while they land form
     // the next chunk's per-step vectors and state copy, then this chunk's outputs
-    const float ei = ex2f(Si * kLog2e);
     if (c + 1 < nch) {
       if (tid == 0) load_chunk(c + 1);
       in_flight = true;
@@ -615,26 +631,21 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       state_copy();
     }
 
-    // ---- y = Yd + exp(S_i) Yo + D x; out = y silu(z).  The tensor-memory loads are
-    // warp-wide (.sync.aligned): every lane takes them, only valid rows store.
+    // ---- y = exp(S_i) Yo + Yd + D x (the two accumulators); out = y silu(z).  The
+    // tensor-memory loads are warp-wide (.sync.aligned): every lane takes them, only
+    // valid rows store.
     {
 #pragma unroll
       for (int c0 = 0; c0 < PB; c0 += 32) {
-        float yd[32], yo[32];
+        float yd[32];
         {
           uint32_t ra[32], rb[32];
-          tmem_ld32_nw(lane_t + Sm::T_G + c0, ra);
-          tmem_ld32_nw(lane_t + Sm::T_G + PB + c0, rb);
-          tmem_wait_ld(ra);
-          tmem_wait_ld(rb);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) yd[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
           tmem_ld32_nw(lane_t + Sm::T_YO + c0, ra);
           tmem_ld32_nw(lane_t + Sm::T_YO + PB + c0, rb);
           tmem_wait_ld(ra);
           tmem_wait_ld(rb);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) yo[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+          for (int j = 0; j < 32; ++j) yd[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -645,8 +656,8 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
           for (int e = 0; e < 4; ++e) {
             const int j = q * 8 + 2 * e;
             const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr[(c0 + j) / 2]));
-            float y0 = fmaf(Dh, xf.x, fmaf(ei, yo[j], yd[j]));
-            float y1 = fmaf(Dh, xf.y, fmaf(ei, yo[j + 1], yd[j + 1]));
+            float y0 = fmaf(Dh, xf.x, yd[j]);
+            float y1 = fmaf(Dh, xf.y, yd[j + 1]);
             if (p.z) {
               const float2 zf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw[e]));
               y0 *= __fdividef(zf.x, 1.f + ex2f(-zf.x * kLog2e));
