@@ -472,21 +472,13 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   };
 
-  // chunk 0's vectors and state copy
-  scan(0);
-  state_copy();
-
-  uint32_t cur = 0;  // phase parity of the chunk in hand
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    const uint32_t par = c & 1;
-    cur = par;
-    const int64_t t0 = (int64_t)c * Q;
-    const bool valid = t0 + i < L;
-
-    // ---- the chunk's inputs; G = C B^T (every wait is decided by all threads together,
-    // so that they leave the loop at the same point)
-    if (!__syncthreads_and(mbar_wait(bar_in, par))) { ok = false; break; }
+  uint32_t cur = 0;  // phase parity of the chunk whose copies and products are in hand
+  // ---- chunk cc's inputs, then G = C B^T into the columns of G (free once the previous
+  // chunk's M X is done).  Every wait is decided by all threads together, so that they
+  // leave the loop at the same point; false: the wait ran out.
+  auto start_g = [&](int cc) -> bool {
+    cur = cc & 1;
+    if (!__syncthreads_and(mbar_wait(bar_in, cur))) return false;
     in_flight = false;
     if (tid == 0) {
       tc_fence_after();
@@ -496,6 +488,19 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       mma_commit(bar_g);
     }
     issued |= 1;
+    return true;
+  };
+
+  // chunk 0's vectors, state copy and G
+  scan(0);
+  state_copy();
+  ok = start_g(0);
+
+#pragma unroll 1
+  for (int c = 0; ok && c < nch; ++c) {
+    const uint32_t par = c & 1;
+    const int64_t t0 = (int64_t)c * Q;
+    const bool valid = t0 + i < L;
 
     // ---- Xw_j = exp(S_last - S_j) step_j x_j (hi, lo); x_i kept for D x_i; z_i fetched
     uint32_t xr[PB / 2];
@@ -623,12 +628,14 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     issued &= ~4;
     tc_fence_after();
     // the tiles are consumed: fetch the next chunk's inputs, and while they land form
-    // the next chunk's per-step vectors and state copy, then this chunk's outputs
+    // the next chunk's per-step vectors and state copy; then issue the next chunk's G,
+    // which runs while this chunk's outputs are formed
     if (c + 1 < nch) {
       if (tid == 0) load_chunk(c + 1);
       in_flight = true;
       scan(c + 1);
       state_copy();
+      if (!start_g(c + 1)) { ok = false; break; }
     }
 
     // ---- y = exp(S_i) Yo + Yd + D x (the two accumulators); out = y silu(z).  The
