@@ -5,7 +5,7 @@
 // cores); "Structured State Space Models and Mamba", section "State Space Duality and
 // Mamba-2" (Y = (L o (C B^T)) V with a 1-semiseparable decay mask L).
 //
-// One CTA (four warps, 128 threads) owns one (batch row, head, block of PB channels)
+// One CTA (eight warps, 256 threads) owns one (batch row, head, block of PB channels)
 // and walks the sequence in chunks of Q = 128 steps, the (N, PB) state of its channels
 // carried in tensor memory.  With S_i the running sum of step * A inside a chunk:
 //   G        = C B^T                                          (Q x Q over N)
@@ -22,8 +22,8 @@
 // descriptors; Xw and the state copy are written by the threads in the no-swizzle
 // core-matrix layout (8 rows x 16 bytes per core matrix).  M never leaves tensor memory:
 // each thread reads its row of G, forms its row of M and writes it back over G as the A
-// operand of M X.  Thread i owns TMEM lane i (row i of every accumulator) for the
-// element-wise work.  The state copy and Xw, held as pairs of bf16 parts, enter their
+// operand of M X.  Threads i and i + 128 own TMEM lane i (row i of every accumulator)
+// for the element-wise work, each with half of the columns (of M: alternate blocks).  The state copy and Xw, held as pairs of bf16 parts, enter their
 // products as one operand twice as wide (the parts side by side), so that one
 // instruction forms both partial products into adjacent accumulator columns; the carried
 // state is held as two accumulators (the sum so far, this chunk's low parts).  The two
@@ -59,7 +59,7 @@ namespace ssd {
 
 constexpr int Q = 128;      // steps per chunk (the M dimension of every product)
 constexpr int P = 64;       // channels per head
-constexpr int NTHR = 128;   // threads per CTA: one per TMEM lane
+constexpr int NTHR = 256;   // threads per CTA: two per TMEM lane (each with half the columns)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // 5-D tensor maps (w values, L rows, blocks of w values, head or group, batch row): one
@@ -228,6 +228,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 16 consecutive fp32 columns of this thread's lane, waited for (the wait names the
+// destinations, so that no use of them is scheduled before it).
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),
+                 "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
+                 "+r"(b[14]), "+r"(b[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -288,6 +320,10 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // warps w and w + 4 share lane quarter qw (TMEM lanes 32 qw ..): each takes half of the
+  // columns of every element-wise phase (channels HP hf .. HP hf + HP - 1)
+  const int qw = warp & 3, hf = warp >> 2;
+  constexpr int HP = PB / 2;
   // batch row fastest: the CTAs resident at one time spread over every batch row, so
   // that they do not all read the same C, B tile from L2 at once
   const int b = (int)(blockIdx.x % (unsigned)p.batch), hb = (int)(blockIdx.x / (unsigned)p.batch);
@@ -326,7 +362,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tbase_s;
-  const uint32_t lane_t = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  const uint32_t lane_t = tmem + ((uint32_t)(qw * 32) << 16);  // this warp's lanes
   bool ok = true;
   int issued = 0;  // products issued and not yet waited for: bit 0 G, 1 C h / B^T Xw, 2 M X
 
@@ -336,18 +372,16 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     const int64_t sb = ((int64_t)b * p.H + h) * P * N;
 #pragma unroll 1
     for (int nb = 0; nb < NP / 128; ++nb) {
-      const int n = nb * 128 + tid;
-#pragma unroll 1
-      for (int c0 = 0; c0 < PB; c0 += 32) {
-        float v[32], zero[32];
+      const int n = nb * 128 + qw * 32 + lane;
+      const int c0 = hf * HP;
+      uint32_t v[HP], zero[HP];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = (p.state_in && n < N) ? p.state[sb + (int64_t)(pc + c0 + j) * N + n] : 0.f;
-          zero[j] = 0.f;
-        }
-        tmem_st32(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
-        tmem_st32(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, zero);
+      for (int j = 0; j < HP; ++j) {
+        v[j] = __float_as_uint((p.state_in && n < N) ? p.state[sb + (int64_t)(pc + c0 + j) * N + n] : 0.f);
+        zero[j] = 0u;
       }
+      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
+      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, zero);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   }
@@ -383,11 +417,11 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   auto off16 = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
 
   // the raw step of this thread's row, one chunk ahead
-  float dt_next = (tid < L) ? __bfloat162float(p.dt[((int64_t)b * L + tid) * p.H + h]) : 0.f;
+  const int i = qw * 32 + lane;  // this thread's row of every Q-row product, and its state row
+  float dt_next = (i < L) ? __bfloat162float(p.dt[((int64_t)b * L + i) * p.H + h]) : 0.f;
 
   // ---- per-step vectors of chunk c: step_i, the running sum S_i of step * A (block
   // scan), the chunk's range of S and the split decay factors (smem: Sv, stepv, bv)
-  const int i = tid;  // this thread's row of every Q-row product, and its state row
   float step = 0.f, Si = 0.f, Slast = 0.f, ai = 0.f;
   bool split = true;
   auto scan = [&](int c) {
@@ -406,9 +440,9 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       if (lane >= off) incl += o;
     }
     __syncthreads();  // the previous chunk's readers of Sv, stepv, bv and red are done
-    if (lane == 31) red[warp] = incl;
+    if (hf == 0 && lane == 31) red[qw] = incl;  // both warps of a quarter hold the same sums
     __syncthreads();
-    for (int w = 0; w < warp; ++w) incl += red[w];
+    for (int w = 0; w < qw; ++w) incl += red[w];
     Si = incl;
     float mn = Si, mx = Si;
 #pragma unroll
@@ -416,12 +450,14 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
-    if (lane == 0) {
-      red[4 + warp] = mn;
-      red[8 + warp] = mx;
+    if (hf == 0 && lane == 0) {
+      red[4 + qw] = mn;
+      red[8 + qw] = mx;
     }
-    Sv[i] = Si;
-    stepv[i] = step;
+    if (hf == 0) {
+      Sv[i] = Si;
+      stepv[i] = step;
+    }
     __syncthreads();
     mn = fminf(fminf(red[4], red[5]), fminf(red[6], red[7]));
     mx = fmaxf(fmaxf(red[8], red[9]), fmaxf(red[10], red[11]));
@@ -430,7 +466,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     split = (mx - mn) <= 160.f;
     const float Sref = 0.5f * (mn + mx);
     ai = ex2f((Si - Sref) * kLog2e);
-    bv[i] = ex2f((Sref - Si) * kLog2e) * step;
+    if (hf == 0) bv[i] = ex2f((Sref - Si) * kLog2e) * step;
   };
   // ---- the state entering a chunk (sum of its two accumulators): its bf16 copy (hi, lo)
   // for C h_prev, then h <- exp(S_last) h into the first accumulator, zeros into the
@@ -440,34 +476,29 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
 #pragma unroll 1
     for (int nb = 0; nb < NP / 128; ++nb) {
       const int n = nb * 128 + i;
-#pragma unroll 1
-      for (int c0 = 0; c0 < PB; c0 += 32) {
-        const uint32_t ta = lane_t + Sm::T_H + nb * 2 * PB + c0;
-        uint32_t ra[32], rb[32];
-        tmem_ld32_nw(ta, ra);
-        tmem_ld32_nw(ta + PB, rb);
-        tmem_wait_ld(ra);
-        tmem_wait_ld(rb);
-        float v[32], zero[32];
+      const int c0 = hf * HP;
+      const uint32_t ta = lane_t + Sm::T_H + nb * 2 * PB + c0;
+      uint32_t ra[HP], rb[HP];
+      tmem_ld16x2(ta, ta + PB, ra, rb);
+      float v[HP];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
-          zero[j] = 0.f;
-        }
+      for (int j = 0; j < HP; ++j) v[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t hi[4], lo[4];
+      for (int cb = 0; cb < HP / 8; ++cb) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split2(v[cb * 8 + 2 * e], v[cb * 8 + 2 * e + 1], hi[e], lo[e]);
-          const uint32_t off = cm(n, (c0 >> 3) + cb, NP);
-          *reinterpret_cast<uint4*>(smem + Sm::H_OFF + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(smem + Sm::H_OFF + NP * PB * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= dl;
-        tmem_st32(ta, v);
-        tmem_st32(ta + PB, zero);
+        for (int e = 0; e < 4; ++e) split2(v[cb * 8 + 2 * e], v[cb * 8 + 2 * e + 1], hi[e], lo[e]);
+        const uint32_t off = cm(n, (c0 >> 3) + cb, NP);
+        *reinterpret_cast<uint4*>(smem + Sm::H_OFF + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + Sm::H_OFF + NP * PB * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        ra[j] = __float_as_uint(v[j] * dl);
+        rb[j] = 0u;
+      }
+      tmem_st16u(ta, ra);
+      tmem_st16u(ta + PB, rb);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   };
@@ -502,27 +533,29 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     const int64_t t0 = (int64_t)c * Q;
     const bool valid = t0 + i < L;
 
-    // ---- Xw_j = exp(S_last - S_j) step_j x_j (hi, lo); x_i kept for D x_i; z_i fetched
-    uint32_t xr[PB / 2];
-    uint4 zv[PB / 8];
+    // ---- Xw_j = exp(S_last - S_j) step_j x_j (hi, lo) for this thread's half of the
+    // channels; x_i kept for D x_i; z_i fetched
+    uint32_t xr[HP / 2];
+    uint4 zv[HP / 8];
 #pragma unroll
-    for (int q = 0; q < PB / 8; ++q) zv[q] = make_uint4(0, 0, 0, 0);
-    const int64_t row = (((int64_t)b * L + t0 + i) * p.H + h) * P + pc;
+    for (int q = 0; q < HP / 8; ++q) zv[q] = make_uint4(0, 0, 0, 0);
+    const int64_t row = (((int64_t)b * L + t0 + i) * p.H + h) * P + pc + hf * HP;  // first channel of the half
     if (p.z && valid) {
 #pragma unroll
-      for (int q = 0; q < PB / 8; ++q) zv[q] = __ldg(reinterpret_cast<const uint4*>(p.z + row) + q);
+      for (int q = 0; q < HP / 8; ++q) zv[q] = __ldg(reinterpret_cast<const uint4*>(p.z + row) + q);
     }
     {
       const float wj = ex2f((Slast - Si) * kLog2e) * step;
 #pragma unroll
-      for (int cb = 0; cb < PB / 8; ++cb) {
+      for (int ch = 0; ch < HP / 8; ++ch) {
+        const int cb = hf * (HP / 8) + ch;  // block of 8 channels
         // row i of x: 64 bytes, its 16-byte pieces permuted by bits 1-2 of the row
         const uint4 v = *reinterpret_cast<const uint4*>(smem + Sm::X_OFF + i * 64 + ((cb ^ ((i >> 1) & 3)) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          xr[cb * 4 + e] = w[e];
+          xr[ch * 4 + e] = w[e];
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
           split2(f.x * wj, f.y * wj, hi[e], lo[e]);
         }
@@ -558,10 +591,10 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     issued &= ~1;
     tc_fence_after();
 #pragma unroll 1
-    for (int J = 0; J < Q / 32; ++J) {
+    for (int J = hf; J < Q / 32; J += 2) {  // the two warps of a quarter take alternate blocks
       const int j0 = J * 32;
       uint32_t mv[32];  // [hi 0-7 | lo 0-7 | hi 8-15 | lo 8-15] of the block's 16 pairs
-      if (J <= warp) {  // warp-uniform: blocks right of the diagonal block are zero
+      if (J <= qw) {  // warp-uniform: blocks right of the diagonal block are zero
         float gv[32];
         tmem_ld32(lane_t + Sm::T_G + j0, gv);
         float m[32];
@@ -578,7 +611,7 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) m[jj] = gv[jj] * ex2f((Si - Sv[j0 + jj]) * kLog2e) * stepv[j0 + jj];
         }
-        if (J == warp) {
+        if (J == qw) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) m[jj] = (j0 + jj <= i) ? m[jj] : 0.f;
         }
@@ -598,17 +631,12 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     tc_fence_after();
     {
       const float ei = ex2f(Si * kLog2e);
+      const uint32_t ta = lane_t + Sm::T_YO + hf * HP;
+      uint32_t ra[HP], rb[HP];
+      tmem_ld16x2(ta, ta + PB, ra, rb);
 #pragma unroll
-      for (int c0 = 0; c0 < PB; c0 += 32) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32_nw(lane_t + Sm::T_YO + c0, ra);
-        tmem_ld32_nw(lane_t + Sm::T_YO + PB + c0, rb);
-        tmem_wait_ld(ra);
-        tmem_wait_ld(rb);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ra[j] = __float_as_uint(ei * (__uint_as_float(ra[j]) + __uint_as_float(rb[j])));
-        tmem_st32u(lane_t + Sm::T_YO + c0, ra);
-      }
+      for (int j = 0; j < HP; ++j) ra[j] = __float_as_uint(ei * (__uint_as_float(ra[j]) + __uint_as_float(rb[j])));
+      tmem_st16u(ta, ra);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     // ---- Yd = M X: M_hi X onto exp(S) C h_prev, M_lo X beside it; A from tensor memory
@@ -642,27 +670,24 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     // tensor-memory loads are warp-wide (.sync.aligned): every lane takes them, only
     // valid rows store.
     {
+      float yd[HP];
+      {
+        uint32_t ra[HP], rb[HP];
+        tmem_ld16x2(lane_t + Sm::T_YO + hf * HP, lane_t + Sm::T_YO + PB + hf * HP, ra, rb);
 #pragma unroll
-      for (int c0 = 0; c0 < PB; c0 += 32) {
-        float yd[32];
-        {
-          uint32_t ra[32], rb[32];
-          tmem_ld32_nw(lane_t + Sm::T_YO + c0, ra);
-          tmem_ld32_nw(lane_t + Sm::T_YO + PB + c0, rb);
-          tmem_wait_ld(ra);
-          tmem_wait_ld(rb);
+        for (int j = 0; j < HP; ++j) yd[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+      }
+      {
+        constexpr int c0 = 0;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) yd[j] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < HP / 8; ++q) {
           uint32_t o[4];
-          const uint4 zq = p.z ? zv[(c0 >> 3) + q] : make_uint4(0, 0, 0, 0);
+          const uint4 zq = p.z ? zv[q] : make_uint4(0, 0, 0, 0);
           const uint32_t zw[4] = {zq.x, zq.y, zq.z, zq.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = q * 8 + 2 * e;
-            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr[(c0 + j) / 2]));
+            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr[j / 2]));
             float y0 = fmaf(Dh, xf.x, yd[j]);
             float y1 = fmaf(Dh, xf.y, yd[j + 1]);
             if (p.z) {
@@ -685,18 +710,14 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     const int64_t sb = ((int64_t)b * p.H + h) * P * N;
 #pragma unroll 1
     for (int nb = 0; nb < NP / 128; ++nb) {
-      const int n = nb * 128 + tid;
-#pragma unroll 1
-      for (int c0 = 0; c0 < PB; c0 += 32) {
-        float v[32], w2[32];
-        tmem_ld32(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
-        tmem_ld32(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, w2);
+      const int n = nb * 128 + i;
+      const int c0 = hf * HP;
+      uint32_t ra[HP], rb[HP];
+      tmem_ld16x2(lane_t + Sm::T_H + nb * 2 * PB + c0, lane_t + Sm::T_H + nb * 2 * PB + PB + c0, ra, rb);
+      if (n < N)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += w2[j];
-        if (n < N)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) p.state[sb + (int64_t)(pc + c0 + j) * N + n] = v[j];
-      }
+        for (int j = 0; j < HP; ++j)
+          p.state[sb + (int64_t)(pc + c0 + j) * N + n] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
     }
   }
   // after a wait that ran out, let the tensor copy and the products still in flight
