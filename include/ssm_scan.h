@@ -281,6 +281,10 @@ uint64_t ssm_kernel_launches(void);
  *                   waits of its successors run out.  Leave it 0 otherwise.
  *   "ssd_legacy"    0 (default): ssm_ssd_fwd runs the tcgen05 kernel; 1: the earlier
  *                   mma.sync kernel (kept for comparison).
+ *   "ssd_split"     0 (default): ssm_ssd_fwd chooses how many parts each sequence is
+ *                   cut into (1 when the sequences fit the resident CTAs); 1, 2 or 4
+ *                   force it (at most the chunks of the sequence).  Other values:
+ *                   SSM_ERR_DIMS.
  * Returns SSM_ERR_DIMS for an unknown name or a negative value.
  */
 int ssm_set_option(const char* name, int64_t value);

@@ -23,7 +23,13 @@
  * chunk (128 steps) in the dual form: within a chunk the masked product
  * (L o C B^T)(step x) on the 5th-generation tensor cores (tcgen05, accumulators in
  * tensor memory, inputs staged by TMA); across chunks the (P, N) state of the
- * head, carried in tensor memory; the expanded state never reaches device memory.
+ * head, carried in tensor memory.  When the (batch row, head, 32-channel block)
+ * sequences outnumber the CTAs the GPU holds at once, each sequence is cut into 2
+ * or 4 parts of consecutive chunks taken in order by persistent CTAs; a part hands
+ * its end state (fp32, P x N per block) to the next through a workspace that the
+ * call takes from the library's stream-ordered pool and returns (SSM_ERR_NOMEM if it
+ * cannot), with a release flag the next part waits for (bounded, 2 s).  The result
+ * is bitwise the same for any number of parts.
  *
  * Conventions as in ssm_scan.h: device pointers on the current device,
  * contiguous row-major, 16-byte aligned, owned by the caller; the call enqueues
@@ -74,7 +80,8 @@ typedef struct {
  * SSM_ERR_DIMS (a size out of range, ngroups not dividing nheads, an unknown flag
  * value, state_in without final_state), SSM_ERR_ALIGN, SSM_ERR_OVERLAP,
  * SSM_ERR_UNSUPPORTED (io dtype, headdim or dstate this build does not cover),
- * SSM_ERR_CUDA (launch failure or no usable device).  A wait inside the kernel
+ * SSM_ERR_CUDA (launch failure or no usable device), SSM_ERR_NOMEM (the workspace
+ * of a call whose sequences are cut into parts).  A wait inside the kernel
  * that does not end within 2 s leaves the call's outputs undefined; the kernel
  * then frees what it holds and returns, and ssm_check_status reports
  * SSM_ERR_TIMEOUT.

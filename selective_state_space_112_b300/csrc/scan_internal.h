@@ -28,6 +28,10 @@ int scan_forward(const void* x, const void* delta, const float* A, const void* B
 // Counts one kernel launch of the library (read by ssm_kernel_launches).
 void count_launch();
 
+// The library's stream-ordered memory pool of device dev (workspaces are taken from it
+// with cudaMallocFromPoolAsync and returned with cudaFreeAsync).
+cudaError_t workspace_pool(int dev, cudaMemPool_t* out);
+
 // Device address of the status word the kernels raise (read by ssm_check_status), or
 // null if the runtime cannot give it.
 int* status_word();

@@ -26,6 +26,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -508,6 +509,7 @@ int launch_ssd(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
 // ------------------------------------------------ the tcgen05 kernel (ssd_tc.cuh)
 
 std::atomic<int64_t> g_ssd_legacy{0};  // 1: the mma.sync kernel above instead
+std::atomic<int64_t> g_ssd_split{0};   // parts per sequence: 0 automatic, else 1, 2 or 4
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -546,15 +548,36 @@ template <int NP, int PB, int N>
 int launch_ssd_tc(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
   using Sm = ssd::Smem<NP, PB>;
   static std::atomic<uint64_t> ready{0};
+  static std::atomic<int> slots_cache[64];  // resident CTAs per device (0: not yet known)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(ready.load() & bit)) {
+    // all of the unified L1 as shared memory: two CTAs of 106 KB per SM at N <= 128
     if (cudaFuncSetAttribute(ssd::ssd_tc_kernel<NP, PB, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Sm::BYTES) != cudaSuccess)
+                             Sm::BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(ssd::ssd_tc_kernel<NP, PB, N>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return SSM_ERR_CUDA;
+    // CTAs resident per SM, from the kernel's registers (allocated per warp in units of
+    // 256), its shared memory (plus the per-block reservation) and its tensor-memory
+    // columns (512 per SM).  (The occupancy calculator answers 1 for this kernel at any
+    // size, which is not what the SM does: the 4-warp build held two CTAs per SM.)
+    cudaFuncAttributes fa;
+    int sms = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0;
+    if (cudaFuncGetAttributes(&fa, ssd::ssd_tc_kernel<NP, PB, N>) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;
+    int per_sm = std::min(regs_sm / (warp_regs * (ssd::NTHR / 32)), smem_sm / (Sm::BYTES + smem_rsv));
+    per_sm = std::min(per_sm, 512 / Sm::TCOLS);
+    slots_cache[dev & 63] = std::max(per_sm, 1) * std::max(sms, 1);
     ready.fetch_or(bit);
   }
+  const int64_t slots = slots_cache[dev & 63].load();
   ssd::Maps maps;
   std::memset(&maps, 0, sizeof maps);
   if (!encode_tile(&maps.x, prm.x, P, prm.H, prm.L, batch, PB, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -568,11 +591,52 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
   p.N = N; p.softplus = prm.softplus; p.state_in = prm.state_in; p.batch = (int)batch;
   p.status = ssm_internal::status_word();
   if (!p.status) return SSM_ERR_CUDA;
-  const int64_t ctas = (int64_t)prm.H * (ssd::P / PB) * batch;
-  if (ctas > INT32_MAX) return SSM_ERR_DIMS;
-  ssd::ssd_tc_kernel<NP, PB, N><<<dim3((unsigned)ctas), ssd::NTHR, Sm::BYTES, stream>>>(maps, p);
+  // Work: `units` (batch row, head, PB channels) sequences.  When they outnumber the
+  // resident CTAs, each is cut into nsplit parts of consecutive chunks taken in order
+  // by persistent CTAs, so that the last round is not left mostly empty.  A part costs
+  // its chunks plus about two chunk times of pipeline start (measured); nsplit (1, 2 or
+  // 4, at most the chunks) minimises rounds x that cost, the smaller on a tie.  Option
+  // ssd_split forces it.
+  const int64_t units = (int64_t)prm.H * (ssd::P / PB) * batch;
+  const int64_t nch = (prm.L + ssd::Q - 1) / ssd::Q;
+  if (units * 4 > INT32_MAX) return SSM_ERR_DIMS;
+  int nsplit = 1;
+  const int64_t forced = g_ssd_split.load();
+  if (forced > 0) {
+    nsplit = (int)forced;
+  } else if (units > slots) {
+    auto cost = [&](int64_t n) { return ((n * units + slots - 1) / slots) * ((nch + n - 1) / n + 2); };
+    for (int n = 2; n <= 4 && n <= nch; n *= 2)
+      if (cost(n) < cost(nsplit)) nsplit = n;
+  }
+  while (nsplit > 1 && nsplit > nch) nsplit /= 2;
+  p.units = (int)units;
+  p.items = (int)(units * nsplit);
+  p.nsplit = nsplit;
+  const bool persistent = p.items > slots || nsplit > 1;
+  void* ws = nullptr;
+  if (persistent) {
+    // workspace: the item counter, a flag per (part, unit) and the carries between parts
+    const size_t nflag = (size_t)(nsplit - 1) * units;
+    const size_t head = ((1 + nflag) * sizeof(int) + 255) / 256 * 256;
+    const size_t bytes = head + nflag * PB * N * sizeof(float);
+    cudaMemPool_t pool;
+    if (ssm_internal::workspace_pool(dev, &pool) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) return SSM_ERR_NOMEM;
+    if (cudaMemsetAsync(ws, 0, head, stream) != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return SSM_ERR_CUDA;
+    }
+    p.counter = static_cast<int*>(ws);
+    p.flags = p.counter + 1;
+    p.carry = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + head);
+  }
+  const int64_t grid = persistent ? std::min<int64_t>(p.items, slots) : p.items;
+  ssd::ssd_tc_kernel<NP, PB, N><<<dim3((unsigned)grid), ssd::NTHR, Sm::BYTES, stream>>>(maps, p);
   ssm_internal::count_launch();
-  return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  int rc = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA;
+  return rc;
 }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -658,6 +722,11 @@ namespace ssm_internal {
 bool set_ssd_option(const char* name, int64_t value) {
   if (!std::strcmp(name, "ssd_legacy")) {
     g_ssd_legacy = value ? 1 : 0;
+    return true;
+  }
+  if (!std::strcmp(name, "ssd_split")) {  // 0: automatic; 1, 2, 4: parts per sequence
+    if (value != 0 && value != 1 && value != 2 && value != 4) return false;
+    g_ssd_split = value;
     return true;
   }
   return false;

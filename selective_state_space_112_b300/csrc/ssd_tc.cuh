@@ -5,9 +5,16 @@
 // cores); "Structured State Space Models and Mamba", section "State Space Duality and
 // Mamba-2" (Y = (L o (C B^T)) V with a 1-semiseparable decay mask L).
 //
-// One CTA (eight warps, 256 threads) owns one (batch row, head, block of PB channels)
-// and walks the sequence in chunks of Q = 128 steps, the (N, PB) state of its channels
-// carried in tensor memory.  With S_i the running sum of step * A inside a chunk:
+// A CTA (eight warps, 256 threads) takes one (batch row, head, block of PB channels) --
+// a unit -- or one part of a unit's sequence, and walks it in chunks of Q = 128 steps,
+// the (N, PB) state of its channels carried in tensor memory.  When the units outnumber
+// the resident CTAs, CTAs persist and take the parts (consecutive chunks) in order from
+// a counter: part s of a unit waits for the release flag of part s - 1 and starts from
+// the state it left (fp32) in a workspace; taking items in order means the part waited
+// for is held by a CTA already running, which never waits on a later item.  The state
+// between parts is the sum of its two accumulators, the value every chunk start forms
+// anyway, so the result does not depend on the number of parts.  With S_i the running
+// sum of step * A inside a chunk:
 //   G        = C B^T                                          (Q x Q over N)
 //   M[i][j]  = G[i][j] exp(S_i - S_j) step_j   for j <= i, else 0
 //   Yd       = M X                                            (Q x PB over Q)
@@ -81,6 +88,15 @@ struct Params {
   __nv_bfloat16* out;
   float* state;       // (batch, H, P, N) or null
   int* status;
+  // work items: each (batch row, head, block of PB channels) -- a unit -- walks its
+  // sequence in nsplit parts of consecutive chunks; item k is part k / units of unit
+  // k % units.  With counter set, CTAs take items in order from it (a part s > 0 waits
+  // for flags[(s - 1) units + u] and starts from the state part s - 1 left in carry
+  // [(s - 1) units + u][PB][N]); without it CTA k runs item k alone (nsplit 1).
+  int* counter;
+  int* flags;
+  float* carry;
+  int units, items, nsplit;
   int64_t L;
   int batch, H, G, hpg, N;
   int softplus, state_in;
@@ -95,7 +111,7 @@ struct Smem {
   static constexpr int X_OFF = B_OFF + Q * NP * 2;       // x tile  [Q x PB]
   static constexpr int W_OFF = X_OFF + Q * PB * 2;       // Xw hi, lo [Q x PB] each
   static constexpr int H_OFF = W_OFF + 2 * Q * PB * 2;   // state hi, lo [NP x PB] each
-  static constexpr int V_OFF = H_OFF + 2 * NP * PB * 2;  // S, step, b (Q floats each), reductions
+  static constexpr int V_OFF = H_OFF + 2 * NP * PB * 2;  // S, step, b (Q floats each), reductions, item
   static constexpr int BAR_OFF = V_OFF + 3 * Q * 4 + 64;
   static constexpr int BYTES = BAR_OFF + 64;
   // TMEM columns: G, then M (hi, lo: two bf16 per column) in its place; C h_hi | C h_lo,
@@ -120,6 +136,16 @@ __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t par) {
@@ -313,7 +339,7 @@ __device__ __forceinline__ uint32_t cm(int r, int cb, int R) { return (uint32_t)
 
 // NN = N (a compile-time state size: the product loops unroll with constant descriptors)
 template <int NP, int PB, int NN>
-__global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::TCOLS <= 256) ? 2 : 1)
+__global__ void __maxnreg__((Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::TCOLS <= 256) ? 120 : 255)
     ssd_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
   static_assert(NN % 64 == 0 && NN <= NP, "state size: a multiple of 64, at most the padded rows");
   using Sm = Smem<NP, PB>;
@@ -324,19 +350,17 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   // columns of every element-wise phase (channels HP hf .. HP hf + HP - 1)
   const int qw = warp & 3, hf = warp >> 2;
   constexpr int HP = PB / 2;
-  // batch row fastest: the CTAs resident at one time spread over every batch row, so
-  // that they do not all read the same C, B tile from L2 at once
-  const int b = (int)(blockIdx.x % (unsigned)p.batch), hb = (int)(blockIdx.x / (unsigned)p.batch);
-  const int h = hb / (P / PB), pc = (hb % (P / PB)) * PB;  // head, first channel
-  const int g = h / p.hpg;
+  // the item in hand: batch row b, head h, first channel pc, group g (set per item)
+  int b = 0, h = 0, pc = 0, g = 0;
+  float Ah = 0.f, Dh = 0.f, biash = 0.f;
   const int64_t L = p.L;
   const int nch = (int)((L + Q - 1) / Q);
   constexpr int N = NN, kN = NN / 16;  // K steps over the state dimension
-  const float Ah = p.A[h], Dh = p.D ? p.D[h] : 0.f, biash = p.dt_bias ? p.dt_bias[h] : 0.f;
   float* Sv = reinterpret_cast<float*>(smem + Sm::V_OFF);  // S_i of the chunk
   float* stepv = Sv + Q;                                  // step_i
   float* bv = stepv + Q;                                  // exp(S_ref - S_j) step_j
   float* red = bv + Q;                                    // per-warp sums, minima, maxima
+  int* item_s = reinterpret_cast<int*>(red + 12);         // the item taken by thread 0
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::BAR_OFF);
   uint32_t* tbase_s = reinterpret_cast<uint32_t*>(bars + 4);
   const uint32_t bar_in = su32(&bars[0]), bar_g = su32(&bars[1]), bar_s = su32(&bars[2]),
@@ -365,30 +389,17 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   const uint32_t lane_t = tmem + ((uint32_t)(qw * 32) << 16);  // this warp's lanes
   bool ok = true;
   int issued = 0;  // products issued and not yet waited for: bit 0 G, 1 C h / B^T Xw, 2 M X
+  uint32_t gc = 0;  // chunks this CTA has begun: each takes one phase of every barrier
 
-  // the state: h_{-1} (or zeros) into its first accumulator, zeros into the second;
-  // lane n = state n, columns of PB channels
-  {
-    const int64_t sb = ((int64_t)b * p.H + h) * P * N;
-#pragma unroll 1
-    for (int nb = 0; nb < NP / 128; ++nb) {
-      const int n = nb * 128 + qw * 32 + lane;
-      const int c0 = hf * HP;
-      uint32_t v[HP], zero[HP];
-#pragma unroll
-      for (int j = 0; j < HP; ++j) {
-        v[j] = __float_as_uint((p.state_in && n < N) ? p.state[sb + (int64_t)(pc + c0 + j) * N + n] : 0.f);
-        zero[j] = 0u;
-      }
-      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
-      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, zero);
-    }
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-  }
-
-  // the inputs of chunk c: C, B (Q x N) and x (Q x PB), one tensor copy each
+  // the inputs of chunk c: C, B (Q x N) and x (Q x PB), one tensor copy each, landing in
+  // barrier phase par
   const uint32_t in_bytes = (uint32_t)((2 * (N / 8) + PB / 8) * Q * 16);
-  auto load_chunk = [&](int c) {
+  bool in_flight = false;  // a tensor copy into the tiles has been issued and not waited for
+  uint32_t in_par = 0;     // ... in this phase of bar_in
+  auto load_chunk = [&](int c, uint32_t par) {
+    in_flight = true;
+    in_par = par;
+    if (tid != 0) return;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_in), "r"(in_bytes)
                  : "memory");
     const int t0 = c * Q;
@@ -396,8 +407,6 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     tma_load_5d(s_base + Sm::B_OFF, &maps.B, 0, t0, 0, g, b, bar_in);
     tma_load_5d(s_base + Sm::X_OFF, &maps.x, 0, t0, pc / PB, h, b, bar_in);
   };
-  if (tid == 0) load_chunk(0);
-  bool in_flight = true;  // a tensor copy into the tiles has been issued and not waited for
 
   constexpr uint32_t ID_G = idesc(Q, Q, 0, 0);          // C (K-major) x B^T (K-major)
   constexpr uint32_t ID_Y = idesc(Q, PB, 0, 1);         // M (TMEM) x X (MN-major)
@@ -416,9 +425,8 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
   auto kmaj = [](int k) { return (uint32_t)((k >> 2) * kAtom + (k & 3) * 32); };
   auto off16 = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
 
-  // the raw step of this thread's row, one chunk ahead
   const int i = qw * 32 + lane;  // this thread's row of every Q-row product, and its state row
-  float dt_next = (i < L) ? __bfloat162float(p.dt[((int64_t)b * L + i) * p.H + h]) : 0.f;
+  float dt_next = 0.f;           // the raw step of this thread's row, one chunk ahead
 
   // ---- per-step vectors of chunk c: step_i, the running sum S_i of step * A (block
   // scan), the chunk's range of S and the split decay factors (smem: Sv, stepv, bv)
@@ -503,13 +511,13 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   };
 
-  uint32_t cur = 0;  // phase parity of the chunk whose copies and products are in hand
-  // ---- chunk cc's inputs, then G = C B^T into the columns of G (free once the previous
-  // chunk's M X is done).  Every wait is decided by all threads together, so that they
-  // leave the loop at the same point; false: the wait ran out.
-  auto start_g = [&](int cc) -> bool {
-    cur = cc & 1;
-    if (!__syncthreads_and(mbar_wait(bar_in, cur))) return false;
+  uint32_t cur = 0;  // phase parity of the chunk whose products are in hand
+  // ---- a chunk's inputs (barrier phase par), then G = C B^T into the columns of G (free
+  // once the previous chunk's M X is done).  Every wait is decided by all threads
+  // together, so that they leave the loop at the same point; false: the wait ran out.
+  auto start_g = [&](uint32_t par) -> bool {
+    cur = par;
+    if (!__syncthreads_and(mbar_wait(bar_in, par))) return false;
     in_flight = false;
     if (tid == 0) {
       tc_fence_after();
@@ -522,14 +530,83 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     return true;
   };
 
-  // chunk 0's vectors, state copy and G
-  scan(0);
-  state_copy();
-  ok = start_g(0);
+  bool first = true;
+#pragma unroll 1
+  for (;;) {
+    // ---- the next item
+    __syncthreads();  // every thread has read the previous item
+    if (tid == 0) *item_s = p.counter ? atomicAdd(p.counter, 1) : (first ? (int)blockIdx.x : p.items);
+    __syncthreads();
+    const int k = *item_s;
+    first = false;
+    if (k >= p.items) break;
+    const int part = k / p.units, u = k - part * p.units;
+    // batch row fastest: the items in hand at one time spread over every batch row, so
+    // that they do not all read the same C, B tile from L2 at once
+    b = u % p.batch;
+    const int hb = u / p.batch;
+    h = hb / (P / PB);
+    pc = (hb % (P / PB)) * PB;
+    g = h / p.hpg;
+    Ah = p.A[h];
+    Dh = p.D ? p.D[h] : 0.f;
+    biash = p.dt_bias ? p.dt_bias[h] : 0.f;
+    const int c_begin = (int)((int64_t)nch * part / p.nsplit), c_end = (int)((int64_t)nch * (part + 1) / p.nsplit);
+
+    // the first chunk's copies and per-step vectors
+    load_chunk(c_begin, gc & 1);
+    {
+      const int64_t t = (int64_t)c_begin * Q + i;
+      dt_next = (t < L) ? __bfloat162float(p.dt[((int64_t)b * L + t) * p.H + h]) : 0.f;
+    }
+    scan(c_begin);
+    // the entering state: h_{-1} or zeros (part 0), else what part - 1 left in the carry
+    const float* src = nullptr;
+    int64_t src_n = 0;  // the stride of a channel in src
+    if (part > 0) {
+      const int* f = p.flags + (size_t)(part - 1) * p.units + u;
+      bool ready = true;
+      if (tid == 0) {
+        ready = ld_acquire(f) != 0;
+        if (!ready) {
+          const uint64_t w0 = gtimer();
+          for (long long it = 0; it < (1ll << 30) && !ready; ++it) {
+            __nanosleep(256);
+            ready = ld_acquire(f) != 0;
+            if (!ready && gtimer() - w0 > kWaitNs) break;
+          }
+        }
+      }
+      if (!__syncthreads_and(ready)) { ok = false; break; }
+      (void)ld_acquire(f);  // every thread acquires the part's release before its reads
+      src = p.carry + ((size_t)(part - 1) * p.units + u) * PB * N;
+      src_n = N;
+    } else if (p.state_in) {
+      src = p.state + (((int64_t)b * p.H + h) * P + pc) * N;
+      src_n = N;
+    }
+    // into the state's first accumulator, zeros into the second; lane n = state n,
+    // columns of PB channels
+#pragma unroll 1
+    for (int nb = 0; nb < NP / 128; ++nb) {
+      const int n = nb * 128 + i;
+      const int c0 = hf * HP;
+      uint32_t v[HP], zero[HP];
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        v[j] = __float_as_uint((src && n < N) ? src[(int64_t)(c0 + j) * src_n + n] : 0.f);
+        zero[j] = 0u;
+      }
+      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + c0, v);
+      tmem_st16u(lane_t + Sm::T_H + nb * 2 * PB + PB + c0, zero);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    state_copy();
+    if (!start_g(gc & 1)) { ok = false; break; }
 
 #pragma unroll 1
-  for (int c = 0; ok && c < nch; ++c) {
-    const uint32_t par = c & 1;
+  for (int c = c_begin; ok && c < c_end; ++c, ++gc) {
+    const uint32_t par = gc & 1;
     const int64_t t0 = (int64_t)c * Q;
     const bool valid = t0 + i < L;
 
@@ -658,12 +735,11 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     // the tiles are consumed: fetch the next chunk's inputs, and while they land form
     // the next chunk's per-step vectors and state copy; then issue the next chunk's G,
     // which runs while this chunk's outputs are formed
-    if (c + 1 < nch) {
-      if (tid == 0) load_chunk(c + 1);
-      in_flight = true;
+    if (c + 1 < c_end) {
+      load_chunk(c + 1, (gc + 1) & 1);
       scan(c + 1);
       state_copy();
-      if (!start_g(c + 1)) { ok = false; break; }
+      if (!start_g((gc + 1) & 1)) { ok = false; break; }
     }
 
     // ---- y = exp(S_i) Yo + Yd + D x (the two accumulators); out = y silu(z).  The
@@ -703,27 +779,39 @@ __global__ void __launch_bounds__(NTHR, (Smem<NP, PB>::BYTES <= 110 * 1024 && Sm
     }
     tc_fence_before();
   }
-  if (!ok && tid == 0) atomicExch(p.status, 1);
+    if (!ok) break;
 
-  // the final state: lane n, columns of PB channels -> state[b, h, pc + j, n]
-  if (ok && p.state) {
-    const int64_t sb = ((int64_t)b * p.H + h) * P * N;
+    // ---- the leaving state (the sum of its two accumulators; lane n, columns of PB
+    // channels): into the carry of part + 1, or the final state[b, h, pc + j, n]
+    const bool to_carry = part + 1 < p.nsplit;
+    if (to_carry || p.state) {
+      float* dst = to_carry ? p.carry + ((size_t)part * p.units + u) * PB * N
+                            : p.state + (((int64_t)b * p.H + h) * P + pc) * N;
 #pragma unroll 1
-    for (int nb = 0; nb < NP / 128; ++nb) {
-      const int n = nb * 128 + i;
-      const int c0 = hf * HP;
-      uint32_t ra[HP], rb[HP];
-      tmem_ld16x2(lane_t + Sm::T_H + nb * 2 * PB + c0, lane_t + Sm::T_H + nb * 2 * PB + PB + c0, ra, rb);
-      if (n < N)
+      for (int nb = 0; nb < NP / 128; ++nb) {
+        const int n = nb * 128 + i;
+        const int c0 = hf * HP;
+        uint32_t ra[HP], rb[HP];
+        tmem_ld16x2(lane_t + Sm::T_H + nb * 2 * PB + c0, lane_t + Sm::T_H + nb * 2 * PB + PB + c0, ra, rb);
+        if (n < N)
 #pragma unroll
-        for (int j = 0; j < HP; ++j)
-          p.state[sb + (int64_t)(pc + c0 + j) * N + n] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+          for (int j = 0; j < HP; ++j) dst[(int64_t)(c0 + j) * N + n] = __uint_as_float(ra[j]) + __uint_as_float(rb[j]);
+      }
+    }
+    if (to_carry) {
+      __syncthreads();  // every thread's carry stores come before the release
+      if (tid == 0) {
+        __threadfence();
+        st_release(p.flags + (size_t)part * p.units + u, 1);
+      }
     }
   }
+  if (!ok && tid == 0) atomicExch(p.status, 1);
+
   // after a wait that ran out, let the tensor copy and the products still in flight
   // finish (each wait bounded) before the shared and tensor memory are released
-  if (!ok && tid == 0) {  // everything outstanding belongs to the chunk the loop left at
-    if (in_flight) mbar_wait(bar_in, cur);
+  if (!ok && tid == 0) {  // the products outstanding belong to one chunk (parity cur)
+    if (in_flight) mbar_wait(bar_in, in_par);
     if (issued & 1) mbar_wait(bar_g, cur);
     if (issued & 2) mbar_wait(bar_s, cur);
     if (issued & 4) mbar_wait(bar_y, cur);

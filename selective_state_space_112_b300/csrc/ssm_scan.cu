@@ -383,6 +383,8 @@ namespace ssm_internal {
 
 void count_launch() { g_launches.fetch_add(1); }
 
+cudaError_t workspace_pool(int dev, cudaMemPool_t* out) { return get_pool(dev, out); }
+
 int* status_word() {
   int* status = nullptr;
   if (cudaGetSymbolAddress((void**)&status, g_status) != cudaSuccess) return nullptr;

@@ -153,6 +153,10 @@ def test_options():
         _abi.set_option("chunks", -1)
     for name in ("chunks", "min_chunk_len", "lanes"):
         _abi.set_option(name, 0)
+    for v in (2, 4, 1, 0):
+        _abi.set_option("ssd_split", v)
+    with pytest.raises(_abi.SSMError):
+        _abi.set_option("ssd_split", 3)
     _abi.set_option("min_chunk_len", 64)
     _abi.set_option("lane_threads", 36864)
     _abi.set_option("ctas_per_sm", 3)

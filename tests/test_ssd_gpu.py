@@ -92,6 +92,38 @@ def test_ssd_fast_decay_takes_the_unsplit_path():
     assert_close(st, ref_st, "bf16", "fast decay: final state")
 
 
+SPLIT_CASES = [
+    ("n64_ragged_parts", dict(batch=2, seqlen=200, nheads=4, headdim=64, dstate=64)),
+    ("n128_groups_state_parts", dict(batch=2, seqlen=700, nheads=6, headdim=64, dstate=128, ngroups=2,
+                                     state_in=True)),
+    ("n256_state_parts", dict(batch=1, seqlen=777, nheads=4, headdim=64, dstate=256, ngroups=2,
+                              state_in=True)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_ssd_sequence_parts(name, kw):
+    """Each sequence cut into 2 and 4 parts of consecutive chunks, taken in order by
+    persistent CTAs with the state handed over through the carry: the result equals
+    the one-part run bit for bit (the carry is the sum of the state's accumulators
+    that every chunk start forms anyway) and the oracle at the bf16 bar."""
+    import selective_state_space_112_b300 as ssm
+    w = make_ssd(name, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    try:
+        ssm.ssm_set_option("ssd_split", 1)
+        out1, st1 = ssd_gpu(w)
+        for parts in (2, 4):
+            ssm.ssm_set_option("ssd_split", parts)
+            out, st = ssd_gpu(w)
+            assert np.array_equal(out, out1), f"{name}: {parts} parts: out"
+            assert np.array_equal(st, st1), f"{name}: {parts} parts: final state"
+    finally:
+        ssm.ssm_set_option("ssd_split", 0)
+    ref, ref_st = ssd_oracle(w)
+    assert_close(out1, ref, "bf16", f"{name}: out")
+    assert_close(st1, ref_st, "bf16", f"{name}: final state")
+
+
 def test_ssd_continuation_and_determinism():
     """Two calls carrying the state equal one call over the whole sequence (the
     split falls inside a chunk), and a repeated call is bitwise identical."""
@@ -164,6 +196,27 @@ def test_ssd_full_size_sampled_heads():
     row and the head range (the first and last head included) against the oracle run
     on that head's slice of the inputs."""
     _full_size_sampled("mamba2_2p7b_bf16", 16, 2700)
+
+
+def test_ssd_full_size_parts_bitwise():
+    """The 2.7B-shaped layer as the benchmark launches it (more sequences than
+    resident CTAs: parts taken in order by persistent CTAs) equals the one-part launch
+    of 640 CTAs and the four-part launch bit for bit."""
+    import torch
+    import selective_state_space_112_b300 as ssm
+    w = make_ssd("mamba2_2p7b_bf16", **SSD_CONFIGS["mamba2_2p7b_bf16"])
+    res = []
+    try:
+        for parts in (0, 1, 4):
+            ssm.ssm_set_option("ssd_split", parts)
+            res.append(ssd_gpu(w))
+    finally:
+        ssm.ssm_set_option("ssd_split", 0)
+    for (o, s), parts in zip(res[1:], (1, 4)):
+        assert np.array_equal(o, res[0][0]), f"{parts} parts: out"
+        assert np.array_equal(s, res[0][1]), f"{parts} parts: final state"
+    del res
+    torch.cuda.empty_cache()
 
 
 def test_ssd_full_size_n256_sampled_heads():
