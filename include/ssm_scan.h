@@ -285,6 +285,10 @@ uint64_t ssm_kernel_launches(void);
  *                   cut into (1 when the sequences fit the resident CTAs); 1, 2 or 4
  *                   force it (at most the chunks of the sequence).  Other values:
  *                   SSM_ERR_DIMS.
+ *   "ssd_hold_part" failure injection for tests (0 = off): with value k and the
+ *                   sequences cut into parts, the first part of unit k - 1 never
+ *                   hands its state over, so the wait of the next part runs out (2 s,
+ *                   SSM_ERR_TIMEOUT).  Leave it 0 otherwise.
  * Returns SSM_ERR_DIMS for an unknown name or a negative value.
  */
 int ssm_set_option(const char* name, int64_t value);

@@ -510,6 +510,7 @@ int launch_ssd(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
 
 std::atomic<int64_t> g_ssd_legacy{0};  // 1: the mma.sync kernel above instead
 std::atomic<int64_t> g_ssd_split{0};   // parts per sequence: 0 automatic, else 1, 2 or 4
+std::atomic<int64_t> g_ssd_hold{0};    // tests: 1 + unit whose first part never hands over
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -610,6 +611,7 @@ int launch_ssd_tc(const SsdParams& prm, int64_t batch, cudaStream_t stream) {
       if (cost(n) < cost(nsplit)) nsplit = n;
   }
   while (nsplit > 1 && nsplit > nch) nsplit /= 2;
+  p.hold_unit = (int)std::min<int64_t>(g_ssd_hold.load(), INT32_MAX) - 1;
   p.units = (int)units;
   p.items = (int)(units * nsplit);
   p.nsplit = nsplit;
@@ -722,6 +724,11 @@ namespace ssm_internal {
 bool set_ssd_option(const char* name, int64_t value) {
   if (!std::strcmp(name, "ssd_legacy")) {
     g_ssd_legacy = value ? 1 : 0;
+    return true;
+  }
+  if (!std::strcmp(name, "ssd_hold_part")) {  // failure injection for tests
+    if (value < 0) return false;
+    g_ssd_hold = value;
     return true;
   }
   if (!std::strcmp(name, "ssd_split")) {  // 0: automatic; 1, 2, 4: parts per sequence

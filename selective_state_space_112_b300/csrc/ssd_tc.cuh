@@ -97,6 +97,7 @@ struct Params {
   int* flags;
   float* carry;
   int units, items, nsplit;
+  int hold_unit;  // failure injection for tests: part 0 of this unit never releases (-1: none)
   int64_t L;
   int batch, H, G, hpg, N;
   int softplus, state_in;
@@ -800,7 +801,7 @@ __global__ void __maxnreg__((Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::
     }
     if (to_carry) {
       __syncthreads();  // every thread's carry stores come before the release
-      if (tid == 0) {
+      if (tid == 0 && !(part == 0 && u == p.hold_unit)) {
         __threadfence();
         st_release(p.flags + (size_t)part * p.units + u, 1);
       }

@@ -157,6 +157,9 @@ def test_options():
         _abi.set_option("ssd_split", v)
     with pytest.raises(_abi.SSMError):
         _abi.set_option("ssd_split", 3)
+    _abi.set_option("ssd_hold_part", 0)
+    with pytest.raises(_abi.SSMError):
+        _abi.set_option("ssd_hold_part", -1)
     _abi.set_option("min_chunk_len", 64)
     _abi.set_option("lane_threads", 36864)
     _abi.set_option("ctas_per_sm", 3)

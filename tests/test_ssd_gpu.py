@@ -124,6 +124,29 @@ def test_ssd_sequence_parts(name, kw):
     assert_close(st1, ref_st, "bf16", f"{name}: final state")
 
 
+def test_ssd_part_handover_timeout_is_reported_and_the_context_stays_usable():
+    """The hand-over between sequence parts without a GPU fault: the first part of one
+    unit is told never to release its state, so the wait of its second part runs out
+    (after 2 s).  The kernel returns, ssm_check_status reports SSM_ERR_TIMEOUT once, and
+    the next call matches the oracle."""
+    import selective_state_space_112_b300 as ssm
+    w = make_ssd("hold_part", batch=1, seqlen=512, nheads=2, headdim=64, dstate=64, seed=31)
+    t = lambda a: to_torch(a)
+    try:
+        ssm.ssm_set_option("ssd_split", 2)
+        ssm.ssm_set_option("ssd_hold_part", 2)
+        ssm.ssm_ssd_fwd(t(w.x), t(w.dt), t(w.A), t(w.B), t(w.C), t(w.D), t(w.z), t(w.dt_bias))
+        assert ssm.ssm_check_status() == -9  # SSM_ERR_TIMEOUT
+        assert ssm.ssm_check_status() == 0
+    finally:
+        ssm.ssm_set_option("ssd_hold_part", 0)
+        ssm.ssm_set_option("ssd_split", 0)
+    out, st = ssd_gpu(w)
+    ref, ref_st = ssd_oracle(w)
+    assert_close(out, ref, "bf16", "after the hand-over timeout: out")
+    assert_close(st, ref_st, "bf16", "after the hand-over timeout: final state")
+
+
 def test_ssd_continuation_and_determinism():
     """Two calls carrying the state equal one call over the whole sequence (the
     split falls inside a chunk), and a repeated call is bitwise identical."""
