@@ -37,12 +37,12 @@
 // parts of M enter as two products (M_hi X onto exp(S_i) C h_prev, M_lo X beside it),
 // summed when the outputs are formed.
 //
-// Order inside a chunk: G is issued as soon as the inputs land; while it runs the
-// threads form Xw, then C h_prev and B^T Xw are issued; M is formed once G is done, the
-// scaled C h_prev written as the start of M X once those two are done, and M X is
-// issued last.  Then the next chunk's copies are issued, and while they land the threads
-// form the next chunk's per-step vectors and state copy (neither needs its inputs) and
-// this chunk's outputs.  The decay factor of M is split as
+// Order inside a chunk (its G already issued): the threads form Xw, then C h_prev and
+// B^T Xw are issued; M is formed once G is done, the scaled C h_prev written as the
+// start of M X once those two are done, and M X is issued last.  Then the next chunk's
+// copies are issued; while they land the threads form its per-step vectors and state
+// copy (neither needs its inputs); then its G is issued, and runs while the threads
+// form this chunk's outputs.  The decay factor of M is split as
 //   exp(S_i - S_j) = exp(S_i - S_ref) exp(S_ref - S_j),  S_ref = the midpoint of the
 // chunk's range of S, so that M costs two multiplies per element; a chunk whose range
 // of S is too wide for both factors to stay inside fp32 takes one exponential per
