@@ -665,11 +665,14 @@ __global__ void __maxnreg__((Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::
     // written over G in tensor memory: per K step of 16 columns of M, 8 columns of packed
     // hi values, then 8 of lo values (a column block of G becomes exactly the two K steps
     // of M it holds, so each warp overwrites only what it has just read)
-    if (!__syncthreads_and(mbar_wait(bar_g, par))) { ok = false; break; }
-    issued &= ~1;
+    // each warp waits for G on its own (its rows of M need nothing else) and the CTA
+    // decides at the next barrier, so that the warps whose threads issue C h_prev and
+    // B^T Xw (their issue waits while the tensor pipe is busy) hold back no other warp
+    const bool g_ok = __all_sync(0xffffffffu, mbar_wait(bar_g, par));
+    if (g_ok) issued &= ~1;
     tc_fence_after();
 #pragma unroll 1
-    for (int J = hf; J < Q / 32; J += 2) {  // the two warps of a quarter take alternate blocks
+    for (int J = hf; g_ok && J < Q / 32; J += 2) {  // the two warps of a quarter take alternate blocks
       const int j0 = J * 32;
       uint32_t mv[32];  // [hi 0-7 | lo 0-7 | hi 8-15 | lo 8-15] of the block's 16 pairs
       if (J <= qw) {  // warp-uniform: blocks right of the diagonal block are zero
@@ -704,7 +707,7 @@ __global__ void __maxnreg__((Smem<NP, PB>::BYTES <= 110 * 1024 && Smem<NP, PB>::
     }
     // ---- the first M X accumulator starts from exp(S_i) C h_prev (C h_hi + C h_lo), in
     // the place of C h_hi; the second starts from zero in the place of C h_lo
-    if (!__syncthreads_and(mbar_wait(bar_s, par))) { ok = false; break; }
+    if (!__syncthreads_and(g_ok && mbar_wait(bar_s, par))) { ok = false; break; }
     issued &= ~2;
     tc_fence_after();
     {
